@@ -1,0 +1,163 @@
+"""CPU oracle for block-sparse FP8 attention prefill (fp64, plain C, ctypes wrapper).
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline leg import this package.  The product library (``block_sparse_fp8_gb300``) never
+does.  The C source, ``bsa_oracle.c``, restates the formula of "Quant Block Sparse Attention"
+(CANNBotDSL, section 算子介绍) and the fixed P-scale online softmax of "hpc-ops Block-Sparse
+FP8 Attention" (section 固定 P-scale 量化技巧); its header lists the readings it takes.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py`` (brute-force
+dense attention, closed forms, invariants, the exhaustive e4m3 table).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sysconfig
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "bsa_oracle.c")
+LIB = os.path.join(HERE, "_build", "libbsa_oracle.so")
+
+EXACT = 0
+PEMU = 1
+
+ERR_BAD_INDEX = 1
+ERR_BAD_PAGE = 2
+ERR_BAD_ARG = 4
+
+
+class OracleDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "B", "N1", "N2", "D", "page_size", "max_q_len", "max_kv_len", "num_pages",
+        "max_pages_per_seq", "total_q", "k_scale_kind", "v_scale_kind", "causal")]
+
+
+class OracleInputs(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_pages", ctypes.c_void_p), ("v_pages", ctypes.c_void_p),
+        ("q_descale", ctypes.c_void_p), ("k_descale", ctypes.c_void_p),
+        ("v_descale", ctypes.c_void_p), ("cu_seqlens_q", ctypes.c_void_p),
+        ("seqused_kv", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+        ("block_mask", ctypes.c_void_p), ("sparse_indices", ctypes.c_void_p),
+        ("sparse_seq_len", ctypes.c_void_p), ("softmax_scale", ctypes.c_double),
+        ("p_scale", ctypes.c_double)]
+
+
+def build(src: str = SRC, out: str = LIB, openmp: bool = True) -> str:
+    """Compiles the oracle with gcc (fp64, no fast-math).  Returns the library path."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+            "-ffp-contract=off", src, "-o", out, "-lm"]
+    if openmp:
+        r = subprocess.run(base[:-3] + ["-fopenmp"] + base[-3:], capture_output=True, text=True)
+        if r.returncode == 0:
+            return out
+    subprocess.run(base, check=True)
+    return out
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    global _lib
+    if path is not None:
+        lib = ctypes.CDLL(path)
+    else:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+            build()
+        lib = ctypes.CDLL(LIB)
+    lib.oracle_e4m3_decode.restype = ctypes.c_double
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+    lib.oracle_active_tiles.restype = ctypes.c_int
+    lib.oracle_active_tiles.argtypes = [ctypes.POINTER(OracleDims), ctypes.POINTER(OracleInputs),
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
+    lib.oracle_all_lists.restype = ctypes.c_int
+    lib.oracle_all_lists.argtypes = [ctypes.POINTER(OracleDims), ctypes.POINTER(OracleInputs),
+                                     ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_attention_rows.restype = ctypes.c_int
+    lib.oracle_attention_rows.argtypes = [ctypes.POINTER(OracleDims),
+                                          ctypes.POINTER(OracleInputs), ctypes.c_int,
+                                          ctypes.c_void_p, ctypes.c_long, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_int]
+    lib.oracle_max_threads.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p).value
+
+
+class Oracle:
+    """Binds one workloads.Case (host arrays) to the C oracle."""
+
+    def __init__(self, case, lib=None):
+        self.case = case
+        self.lib = lib if lib is not None else load()
+        c = case
+        self._keep = [np.ascontiguousarray(a) if a is not None else None for a in (
+            c.q, c.k_pages, c.v_pages, c.q_descale, c.k_descale, c.v_descale, c.cu_seqlens_q,
+            c.seqused_kv, c.block_table, c.block_mask, c.sparse_indices, c.sparse_seq_len)]
+        self.dims = OracleDims(**c.dims())
+        k = self._keep
+        self.inputs = OracleInputs(
+            _ptr(k[0]), _ptr(k[1]), _ptr(k[2]), _ptr(k[3]), _ptr(k[4]), _ptr(k[5]),
+            _ptr(k[6]), _ptr(k[7]), _ptr(k[8]), _ptr(k[9]), _ptr(k[10]), _ptr(k[11]),
+            float(c.softmax_scale), float(c.p_scale))
+
+    def lists(self):
+        """(lists [B,N1,Qb,Kb] int32 with -1 past the count, counts [B,N1,Qb] int32, err)."""
+        c = self.case
+        lists = np.full((c.B, c.N1, c.Qb, c.Kb), -1, dtype=np.int32)
+        counts = np.zeros((c.B, c.N1, c.Qb), dtype=np.int32)
+        err = self.lib.oracle_all_lists(ctypes.byref(self.dims), ctypes.byref(self.inputs),
+                                        _ptr(lists), _ptr(counts))
+        return lists, counts, err
+
+    def rows(self, rows, mode=EXACT, nthreads=0):
+        """rows: int array [n, 2] of (token, head).  Returns (o [n,128] f64, lse [n] f64, err)."""
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+        n = rows.shape[0]
+        o = np.zeros((n, 128), dtype=np.float64)
+        lse = np.zeros(n, dtype=np.float64)
+        err = self.lib.oracle_attention_rows(ctypes.byref(self.dims), ctypes.byref(self.inputs),
+                                             mode, _ptr(rows), n, _ptr(o), _ptr(lse), nthreads)
+        return o, lse, err
+
+    def all_rows(self, mode=EXACT, nthreads=0):
+        """Full O [T, N1, 128] and LSE [N1, T]."""
+        c = self.case
+        tok, h = np.meshgrid(np.arange(c.T), np.arange(c.N1), indexing="ij")
+        rows = np.stack([tok.ravel(), h.ravel()], axis=1)
+        o, lse, err = self.rows(rows, mode, nthreads)
+        return o.reshape(c.T, c.N1, 128), lse.reshape(c.T, c.N1).T.copy(), err
+
+
+def e4m3_decode(code: int) -> float:
+    return load().oracle_e4m3_decode(code)
+
+
+def e4m3_encode(x: float) -> int:
+    return load().oracle_e4m3_encode(x)
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return sysconfig.get_platform()

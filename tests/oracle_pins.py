@@ -1,0 +1,511 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Every pin takes a loaded oracle library (``oracle.load(path)``) so that the same pins can be
+run against deliberately broken builds of the oracle (tests/test_oracle_mutants.py).
+
+What the pins compare against:
+  * the OCP E4M3 table (tests/golden/e4m3_points.json) and PyTorch's float8_e4m3fn cast;
+  * brute-force dense softmax attention written as matrix algebra (numpy + scipy logsumexp)
+    over page-free, token-ordered copies of K and V, with the tile mask expanded to a dense
+    [q, kv] boolean matrix -- none of the oracle's page, list or kend logic;
+  * closed forms (K = 0 gives uniform weights; constant V; the first causal row);
+  * invariances the method must have (masked tiles never read, page permutation, index list
+    vs block mask, GQA replication, p_scale independence of the exact result, zero-filled
+    tails, empty tasks);
+  * a hand-derived fixed-P-scale example for the e4m3-emulating mode.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+from scipy.special import logsumexp
+
+import oracle as O
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+NEG_FLT_MAX = -3.4028234663852886e38
+
+
+def _oracle(case, lib):
+    return O.Oracle(case, lib=lib)
+
+
+def torch_decode(codes: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn)
+    return t.to(torch.float32).numpy().astype(np.float64)
+
+
+# ----------------------------------------------------------------------------------------
+# brute-force reference (independent of the oracle's page / list code)
+# ----------------------------------------------------------------------------------------
+
+def tile_sets(case):
+    """Python sets of enabled KV tiles per (b, h, qt) straight from the mask inputs."""
+    B, N1, Qb, Kb = case.B, case.N1, case.Qb, case.Kb
+    sets = {}
+    for b in range(B):
+        for h in range(N1):
+            for qt in range(Qb):
+                if case.block_mask is not None:
+                    sets[b, h, qt] = {t for t in range(Kb) if case.block_mask[b, h, qt, t]}
+                elif case.sparse_indices is not None:
+                    n = int(case.sparse_seq_len[b, h, qt])
+                    sets[b, h, qt] = {int(t) for t in case.sparse_indices[b, h, qt, :n]}
+                else:
+                    sets[b, h, qt] = set(range(Kb))
+    return sets
+
+
+def brute_force(case):
+    """Dense softmax attention with an explicit [q, kv] allowed-matrix; O [T,N1,D], LSE [N1,T]."""
+    k_codes = case.meta["k_codes"]
+    v_codes = case.meta["v_codes"]
+    Q = torch_decode(case.q) * case.q_descale[..., None].astype(np.float64)
+    K = torch_decode(k_codes)
+    if case.k_scale_kind == W.SCALE_PER_TOKEN_HEAD:
+        K = K * case.meta["k_descale_tok"][..., None].astype(np.float64)
+    else:
+        K = K * float(case.k_descale[0])
+    V = torch_decode(v_codes)
+    if case.v_scale_kind == W.SCALE_PER_HEAD:
+        V = V * case.v_descale[None, :, None].astype(np.float64)
+    else:
+        V = V * float(case.v_descale[0])
+    G = case.N1 // case.N2
+    sets = tile_sets(case)
+    out = np.zeros((case.T, case.N1, W.HEAD_DIM))
+    lse = np.full((case.N1, case.T), NEG_FLT_MAX)
+    kv0 = 0
+    for b in range(case.B):
+        ql, kl = case.q_lens[b], case.kv_lens[b]
+        q0 = int(case.cu_seqlens_q[b])
+        i = np.arange(ql)[:, None]
+        j = np.arange(kl)[None, :]
+        for h in range(case.N1):
+            g = h // G
+            S = case.softmax_scale * (Q[q0:q0 + ql, h] @ K[kv0:kv0 + kl, g].T)
+            allowed = np.ones((ql, kl), dtype=bool)
+            if case.causal:
+                allowed &= j <= i + (kl - ql)
+            tm = np.zeros((max(case.Qb, 1), max(case.Kb, 1)), dtype=bool)
+            for qt in range(case.Qb):
+                for t in sets[b, h, qt]:
+                    if 0 <= t < case.Kb:
+                        tm[qt, t] = True
+            allowed &= tm[i // W.TILE, j // W.TILE]
+            S = np.where(allowed, S, -np.inf)
+            has = allowed.any(axis=1)
+            if has.any():
+                ls = logsumexp(S[has], axis=1)
+                P = np.exp(S[has] - ls[:, None])
+                out[q0 + np.nonzero(has)[0], h] = P @ V[kv0:kv0 + kl, g]
+                lse[h, q0 + np.nonzero(has)[0]] = ls
+        kv0 += kl
+    return out, lse
+
+
+def _close(a, b, tol=1e-9):
+    a = np.asarray(a)
+    b = np.asarray(b)
+    assert a.shape == b.shape, (a.shape, b.shape)
+    err = np.abs(a - b)
+    lim = tol * (1.0 + np.abs(b))
+    assert np.all(err <= lim), f"max err {err.max()} at {np.unravel_index(err.argmax(), err.shape)}"
+
+
+# ----------------------------------------------------------------------------------------
+# e4m3 codec
+# ----------------------------------------------------------------------------------------
+
+def pin_e4m3_spec_points(lib):
+    with open(os.path.join(GOLDEN, "e4m3_points.json")) as f:
+        pts = json.load(f)["points"]
+    for p in pts:
+        c = int(p["code"], 16)
+        v = lib.oracle_e4m3_decode(c)
+        if p["value"] == "nan":
+            assert math.isnan(v), p
+        else:
+            assert v == p["value"] and math.copysign(1, v) == math.copysign(1, p["value"]), (p, v)
+
+
+def pin_e4m3_decode_all_codes(lib):
+    ref = torch_decode(np.arange(256, dtype=np.uint8))
+    for c in range(256):
+        v = lib.oracle_e4m3_decode(c)
+        if math.isnan(ref[c]):
+            assert math.isnan(v), c
+        else:
+            assert v == ref[c] and math.copysign(1, v) == math.copysign(1, ref[c]), (c, v, ref[c])
+
+
+def pin_e4m3_encode(lib):
+    # every finite code round-trips
+    for c in range(256):
+        v = lib.oracle_e4m3_decode(c)
+        if not math.isnan(v):
+            assert lib.oracle_e4m3_encode(v) == c, (hex(c), v)
+    # midpoints between neighbouring codes (ties) and random values agree with torch's RNE
+    fin = sorted({torch_decode(np.array([c], np.uint8))[0] for c in range(256)} - {float("nan")})
+    fin = [x for x in fin if not math.isnan(x)]
+    mids = [(a + b) / 2 for a, b in zip(fin[:-1], fin[1:])]
+    rng = np.random.default_rng(7)
+    rnd = list(rng.standard_normal(3000) * 40) + list(rng.standard_normal(1000) * 0.01)
+    xs = np.array(mids + rnd + [447.9, 440.0, 1e-30, -1e-30], dtype=np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for x, r in zip(xs, ref):
+        assert lib.oracle_e4m3_encode(float(x)) == r, (float(x), hex(r))
+    # saturation (the cast used for P is satfinite)
+    assert lib.oracle_e4m3_encode(1e6) == 0x7E
+    assert lib.oracle_e4m3_encode(-1e6) == 0xFE
+    assert lib.oracle_e4m3_encode(float("inf")) == 0x7E
+    assert lib.oracle_e4m3_encode(470.0) == 0x7E
+    assert lib.oracle_e4m3_encode(float("nan")) & 0x7F == 0x7F
+
+
+# ----------------------------------------------------------------------------------------
+# lists
+# ----------------------------------------------------------------------------------------
+
+def _small_cases():
+    return [
+        W.make_case("bern", 11, [300, 129, 1], [300, 129, 1], 4, 2, 64,
+                    W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD, "bernoulli", keep=0.5,
+                    keep_logical=True),
+        W.make_case("chunk", 12, [200], [700], 2, 1, 32, mask="local_sink", n_local=1,
+                    p_far=0.3, keep_logical=True),
+        W.make_case("idx", 13, [520, 260], [520, 260], 4, 1, 32, W.SCALE_PER_TOKEN_HEAD,
+                    W.SCALE_PER_HEAD, "indices", sparse_frac=0.5, n_empty=1, keep_logical=True),
+        W.make_case("dense", 14, [257], [257], 2, 2, 64, mask="none", keep_logical=True),
+        W.make_case("qlong", 15, [300], [170], 2, 1, 64, mask="ones", keep_logical=True),
+        W.make_case("noncausal", 16, [200, 140], [330, 140], 4, 2, 32, W.SCALE_PER_TOKEN_HEAD,
+                    W.SCALE_PER_HEAD, "ones", causal=0, keep_logical=True),
+    ]
+
+
+_CASES = None
+
+
+def small_cases():
+    global _CASES
+    if _CASES is None:
+        _CASES = _small_cases()
+    return _CASES
+
+
+def pin_lists_vs_sets(lib):
+    """A tile is listed iff it is enabled and holds a key some row of the task can see."""
+    for case in small_cases():
+        lists, counts, err = _oracle(case, lib).lists()
+        assert err == 0
+        sets = tile_sets(case)
+        for b in range(case.B):
+            ql, kl = case.q_lens[b], case.kv_lens[b]
+            for h in range(case.N1):
+                for qt in range(case.Qb):
+                    rows = range(qt * W.TILE, min(ql, qt * W.TILE + W.TILE))
+                    want = []
+                    for t in sorted(sets[b, h, qt]):
+                        if not 0 <= t < case.Kb:
+                            continue
+                        keys = range(t * W.TILE, min(kl, t * W.TILE + W.TILE))
+                        if any((not case.causal) or k <= r + (kl - ql) for r in rows for k in keys):
+                            want.append(t)
+                    got = lists[b, h, qt, :counts[b, h, qt]].tolist()
+                    assert got == want, (case.name, b, h, qt, got, want)
+                    assert np.all(lists[b, h, qt, counts[b, h, qt]:] == -1)
+
+
+# ----------------------------------------------------------------------------------------
+# attention results
+# ----------------------------------------------------------------------------------------
+
+def pin_brute_force(lib):
+    for case in small_cases():
+        o, lse, err = _oracle(case, lib).all_rows(O.EXACT)
+        assert err == 0
+        bo, blse = brute_force(case)
+        _close(o, bo)
+        _close(lse, blse)
+
+
+def pin_ones_equals_dense(lib):
+    a = W.make_case("a", 21, [300, 90], [300, 400], 4, 2, 64, W.SCALE_PER_TOKEN_HEAD,
+                    W.SCALE_PER_HEAD, "ones")
+    b = W.make_case("b", 21, [300, 90], [300, 400], 4, 2, 64, W.SCALE_PER_TOKEN_HEAD,
+                    W.SCALE_PER_HEAD, "none")
+    oa, la, _ = _oracle(a, lib).all_rows()
+    ob, lb, _ = _oracle(b, lib).all_rows()
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+def _uniform_k_case(seed, pemu_exact=True):
+    c = W.make_case("k0", seed, [260, 70], [260, 330], 4, 2, 32, mask="bernoulli", keep=0.6,
+                    keep_logical=True)
+    c.k_pages[:] = 0
+    return c
+
+
+def pin_closed_form_zero_k(lib):
+    """K = 0: every visible key has weight 1/|A_i|, LSE = ln |A_i| (both modes)."""
+    case = _uniform_k_case(31)
+    sets = tile_sets(case)
+    V = torch_decode(case.meta["v_codes"]) * float(case.v_descale[0])
+    G = case.N1 // case.N2
+    for mode in (O.EXACT, O.PEMU):
+        o, lse, _ = _oracle(case, lib).all_rows(mode)
+        kv0 = 0
+        for b in range(case.B):
+            ql, kl = case.q_lens[b], case.kv_lens[b]
+            q0 = int(case.cu_seqlens_q[b])
+            for h in range(case.N1):
+                for i in range(ql):
+                    vis = [j for j in range(kl) if j <= i + kl - ql and (j // 128) in sets[b, h, i // 128]]
+                    if not vis:
+                        assert lse[h, q0 + i] == NEG_FLT_MAX and not o[q0 + i, h].any()
+                        continue
+                    want = V[[kv0 + j for j in vis], h // G].mean(axis=0)
+                    _close(o[q0 + i, h], want, 1e-12)
+                    assert abs(lse[h, q0 + i] - math.log(len(vis))) < 1e-12
+            kv0 += kl
+
+
+def pin_closed_form_const_v(lib):
+    """Every V row equal to c gives O_i = c * v_descale for every row with a visible key."""
+    case = W.make_case("cv", 32, [200], [200], 2, 1, 64, W.SCALE_PER_TOKEN_HEAD,
+                       W.SCALE_PER_HEAD, "bernoulli", keep=0.7)
+    row = np.arange(128, dtype=np.uint8) % 0x70          # a fixed pattern of finite codes
+    case.v_pages[:] = row
+    want = torch_decode(row) * float(case.v_descale[0])
+    o, lse, _ = _oracle(case, lib).all_rows(O.EXACT)
+    for tok in range(case.T):
+        for h in range(case.N1):
+            _close(o[tok, h], want, 1e-12)
+
+
+def pin_first_row(lib):
+    """Row 0 of a sequence with kv_len = q_len sees only key 0: O_0 = V^_0, LSE_0 = s_00."""
+    case = W.make_case("r0", 33, [150, 40], [150, 40], 4, 2, 64, W.SCALE_PER_TOKEN_HEAD,
+                       W.SCALE_PER_HEAD, "bernoulli", keep_logical=True)
+    o, lse, _ = _oracle(case, lib).all_rows()
+    Q = torch_decode(case.q) * case.q_descale[..., None]
+    K = torch_decode(case.meta["k_codes"]) * case.meta["k_descale_tok"][..., None]
+    V = torch_decode(case.meta["v_codes"]) * case.v_descale[None, :, None]
+    kv0 = 0
+    for b in range(case.B):
+        q0 = int(case.cu_seqlens_q[b])
+        for h in range(case.N1):
+            g = h // 2
+            _close(o[q0, h], V[kv0, g], 1e-12)
+            s00 = case.softmax_scale * float(Q[q0, h] @ K[kv0, g])
+            assert abs(lse[h, q0] - s00) < 1e-12 * (1 + abs(s00))
+        kv0 += case.kv_lens[b]
+
+
+def pin_masked_tiles_never_read(lib):
+    """Pages of tiles that no task of a KV group enables are filled with e4m3 NaN: O unchanged."""
+    case = W.make_case("poison", 34, [256], [1024], 4, 2, 64, mask="local_sink", n_local=0,
+                       p_far=0.0)
+    o_ref, l_ref, _ = _oracle(case, lib).all_rows()
+    used = set()
+    G = case.N1 // case.N2
+    for (b, h, qt), s in tile_sets(case).items():
+        used |= {(h // G, t) for t in s}
+    ps = case.page_size
+    n_poison = 0
+    for g in range(case.N2):
+        for t in range(case.Kb):
+            if (g, t) in used:
+                continue
+            for lp in range(t * 128 // ps, (t + 1) * 128 // ps):
+                pg = case.block_table[0, lp]
+                case.k_pages[pg, g] = 0x7F
+                case.v_pages[pg, g] = 0x7F
+                n_poison += 1
+    assert n_poison > 0
+    o, l, _ = _oracle(case, lib).all_rows()
+    assert np.array_equal(o, o_ref) and np.array_equal(l, l_ref)
+
+
+def pin_page_permutation(lib):
+    kw = dict(q_lens=[300, 77], kv_lens=[300, 500], N1=4, N2=2, page_size=32,
+              k_scale_kind=W.SCALE_PER_TOKEN_HEAD, v_scale_kind=W.SCALE_PER_HEAD)
+    a = W.make_case("perm", 35, identity_pages=True, **kw)
+    b = W.make_case("perm", 35, identity_pages=False, **kw)
+    assert not np.array_equal(a.block_table, b.block_table)
+    oa, la, _ = _oracle(a, lib).all_rows()
+    ob, lb, _ = _oracle(b, lib).all_rows()
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+def pin_indices_equal_mask(lib):
+    m = W.make_case("m", 36, [400, 130], [400, 130], 4, 2, 64, mask="bernoulli", keep=0.4)
+    rng = np.random.default_rng(36)
+    idx = np.full(m.block_mask.shape, -1, dtype=np.int32)
+    n = np.zeros(m.block_mask.shape[:3], dtype=np.int32)
+    for key in np.ndindex(*m.block_mask.shape[:3]):
+        on = np.nonzero(m.block_mask[key])[0]
+        rng.shuffle(on)
+        idx[key][:len(on)] = on
+        n[key] = len(on)
+    s = W.make_case("m", 36, [400, 130], [400, 130], 4, 2, 64, mask="none")
+    s.sparse_indices, s.sparse_seq_len = idx, n
+    om, lm = _oracle(m, lib), _oracle(s, lib)
+    la, ca, _ = om.lists()
+    lb, cb, _ = lm.lists()
+    assert np.array_equal(la, lb) and np.array_equal(ca, cb)
+    oa, xa, _ = om.all_rows()
+    ob, xb, _ = lm.all_rows()
+    assert np.array_equal(oa, ob) and np.array_equal(xa, xb)
+
+
+def pin_gqa_replicated(lib):
+    """N1 = 4, N2 = 2 equals N1 = 4, N2 = 4 with KV heads (0, 0, 1, 1)."""
+    g2 = W.make_case("g", 37, [260], [260], 4, 2, 64, W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD,
+                     "bernoulli")
+    g1 = W.make_case("g", 37, [260], [260], 4, 2, 64, W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD,
+                     "bernoulli")
+    rep = [0, 0, 1, 1]
+    g1.N2 = 4
+    g1.k_pages = np.ascontiguousarray(g2.k_pages[:, rep])
+    g1.v_pages = np.ascontiguousarray(g2.v_pages[:, rep])
+    g1.k_descale = np.ascontiguousarray(g2.k_descale[:, rep])
+    g1.v_descale = np.ascontiguousarray(g2.v_descale[rep])
+    oa, la, _ = _oracle(g2, lib).all_rows()
+    ob, lb, _ = _oracle(g1, lib).all_rows()
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+def pin_exact_independent_of_pscale(lib):
+    a = W.make_case("p", 38, [200], [200], 2, 1, 64, mask="bernoulli")
+    b = W.make_case("p", 38, [200], [200], 2, 1, 64, mask="bernoulli", p_scale=100.5)
+    oa, la, _ = _oracle(a, lib).all_rows()
+    ob, lb, _ = _oracle(b, lib).all_rows()
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+def pin_empty_tasks(lib):
+    case = W.make_case("e", 39, [300, 200], [300, 200], 4, 1, 32, mask="indices",
+                       sparse_frac=0.5, n_empty=3)
+    _, counts, _ = _oracle(case, lib).lists()
+    o, lse, _ = _oracle(case, lib).all_rows(O.EXACT)
+    o2, lse2, _ = _oracle(case, lib).all_rows(O.PEMU)
+    empties = 0
+    for b in range(case.B):
+        q0 = int(case.cu_seqlens_q[b])
+        for h in range(case.N1):
+            for qt in range(-(-case.q_lens[b] // 128)):
+                if case.sparse_seq_len[b, h, qt] == 0:
+                    empties += 1
+                    assert counts[b, h, qt] == 0
+                    r = slice(q0 + qt * 128, q0 + min(case.q_lens[b], qt * 128 + 128))
+                    for oo, ll in ((o, lse), (o2, lse2)):
+                        assert not oo[r, h].any()
+                        assert np.all(ll[h, r] == NEG_FLT_MAX)
+    assert empties == 3
+
+
+def pin_tail_slots_unused(lib):
+    kw = dict(q_lens=[300, 100], kv_lens=[300, 100], N1=2, N2=1, page_size=64,
+              k_scale_kind=W.SCALE_PER_TOKEN_HEAD, v_scale_kind=W.SCALE_PER_HEAD, mask="ones")
+    a = W.make_case("t", 40, **kw)
+    b = W.make_case("t", 40, tail_fill=1.0, **kw)
+    assert not np.array_equal(a.k_pages, b.k_pages)
+    for mode in (O.EXACT, O.PEMU):
+        oa, la, _ = _oracle(a, lib).all_rows(mode)
+        ob, lb, _ = _oracle(b, lib).all_rows(mode)
+        assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+def _two_key_case():
+    """T = 2, one head; q = e0, k_0 = 0, k_1 = -e0, v_0 = 1, v_1 = 2, softmax_scale = 0.1."""
+    q = np.zeros((2, 1, 128), np.uint8)
+    q[:, 0, 0] = 0x38                                     # 1.0
+    kp = np.zeros((1, 1, 32, 128), np.uint8)
+    kp[0, 0, 1, 0] = 0xB8                                 # -1.0
+    vp = np.zeros((1, 1, 32, 128), np.uint8)
+    vp[0, 0, 0, :] = 0x38                                 # 1.0
+    vp[0, 0, 1, :] = 0x40                                 # 2.0
+    return W.Case(name="two", B=1, N1=1, N2=1, page_size=32, q_lens=[2], kv_lens=[2],
+                  k_scale_kind=0, v_scale_kind=0, causal=1, softmax_scale=0.1, p_scale=256.0,
+                  q=q, k_pages=kp, v_pages=vp, q_descale=np.ones((2, 1), np.float32),
+                  k_descale=np.ones(1, np.float32), v_descale=np.ones(1, np.float32),
+                  cu_seqlens_q=np.array([0, 2], np.int32), seqused_kv=np.array([2], np.int32),
+                  block_table=np.array([[0]], np.int32),
+                  block_mask=np.ones((1, 1, 1, 1), np.uint8))
+
+
+def pin_fixed_pscale_worked_example(lib):
+    """Row 1 sees s = (0, -0.1).  Exact: O = (1 + 2e^-0.1)/(1 + e^-0.1).  With P-scale 256:
+    p = (1, e^-0.1 = 0.904837...), 256p = (256, 231.638...); 231.638 lies below the midpoint 232
+    of the e4m3 neighbours 224 and 240, so it becomes 224, and
+    O = (256*1 + 224*2) / (256 * (1 + e^-0.1)) = 704 / (256 * 1.904837...).
+    Row 0 sees only key 0: O = 1, LSE = 0."""
+    case = _two_key_case()
+    e = math.exp(-0.1)
+    o, lse, _ = _oracle(case, lib).all_rows(O.EXACT)
+    assert abs(o[1, 0, 0] - (1 + 2 * e) / (1 + e)) < 1e-12
+    assert abs(lse[0, 1] - math.log(1 + math.exp(-0.1))) < 1e-9
+    assert o[0, 0, 5] == 1.0 and lse[0, 0] == 0.0
+    o2, lse2, _ = _oracle(case, lib).all_rows(O.PEMU)
+    assert abs(o2[1, 0, 7] - 704.0 / (256.0 * (1 + e))) < 1e-6
+    assert abs(lse2[0, 1] - math.log(1 + e)) < 1e-6
+    assert o2[0, 0, 0] == 1.0 and lse2[0, 0] == 0.0
+
+
+def _two_tile_case():
+    """256 keys, one head, q = e0, softmax_scale 0.1.  Keys 0..127 (tile 0): k = 0, v = 1.
+    Keys 128..255 (tile 1): k = -e0, v = 2.  So s = 0 on tile 0 and -0.1 on tile 1."""
+    q = np.zeros((256, 1, 128), np.uint8)
+    q[:, 0, 0] = 0x38
+    kp = np.zeros((4, 1, 64, 128), np.uint8)
+    vp = np.zeros((4, 1, 64, 128), np.uint8)
+    kp[2:, 0, :, 0] = 0xB8                                # -1.0 on pages of tile 1
+    vp[:2] = 0x38                                         # 1.0
+    vp[2:] = 0x40                                         # 2.0
+    return W.Case(name="two_tiles", B=1, N1=1, N2=1, page_size=64, q_lens=[256],
+                  kv_lens=[256], k_scale_kind=0, v_scale_kind=0, causal=1, softmax_scale=0.1,
+                  p_scale=256.0, q=q, k_pages=kp, v_pages=vp,
+                  q_descale=np.ones((256, 1), np.float32), k_descale=np.ones(1, np.float32),
+                  v_descale=np.ones(1, np.float32), cu_seqlens_q=np.array([0, 256], np.int32),
+                  seqused_kv=np.array([256], np.int32),
+                  block_table=np.array([[0, 1, 2, 3]], np.int32),
+                  block_mask=np.ones((1, 1, 2, 2), np.uint8))
+
+
+def pin_fixed_pscale_running_max(lib):
+    """Row 255 sees all 256 keys, tile 0 first.  The running max after tile 0 is 0 and stays 0
+    (tile 1's scores are -0.1), so tile 1's p = e^-0.1 is scaled to 231.638... and rounds to
+    224: O = (128*256*1 + 128*224*2) / (256 * (128 + 128 e^-0.1)) = 704 / (256 (1 + e^-0.1)),
+    LSE = ln(128 (1 + e^-0.1)).  The sum l is over the unrounded p.  Row 127 sees tile 0
+    only: O = 1, LSE = ln 128."""
+    case = _two_tile_case()
+    e = math.exp(float(np.float32(-0.1)))
+    o, lse, _ = _oracle(case, lib).all_rows(O.PEMU)
+    assert abs(o[255, 0, 3] - 704.0 / (256.0 * (1 + e))) < 1e-6
+    assert abs(lse[0, 255] - math.log(128 * (1 + e))) < 1e-6
+    assert abs(o[127, 0, 9] - 1.0) < 1e-12 and abs(lse[0, 127] - math.log(128)) < 1e-12
+    o, lse, _ = _oracle(case, lib).all_rows(O.EXACT)
+    ee = math.exp(-0.1)
+    assert abs(o[255, 0, 3] - (1 + 2 * ee) / (1 + ee)) < 1e-12
+
+
+def pin_pemu_near_exact(lib):
+    """The e4m3-rounded P stays within the exact band on all but a sliver of elements."""
+    case = W.make_case("pe", 41, [512], [512], 4, 1, 64, W.SCALE_PER_TOKEN_HEAD,
+                       W.SCALE_PER_HEAD, "bernoulli")
+    a = _oracle(case, lib)
+    o, l, _ = a.all_rows(O.EXACT)
+    o2, l2, _ = a.all_rows(O.PEMU)
+    bad = np.abs(o2 - o) > 0.02 + 0.02 * np.abs(o)
+    assert bad.mean() < 0.005
+    assert np.abs(o2 - o).max() > 1e-4          # the rounding is really applied
+    assert np.all(np.abs(l2 - l) <= 2.5e-5 + 0.005 * np.abs(l))
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
