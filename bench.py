@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark: block-sparse FP8 attention prefill over a paged KV cache on GB300.
+
+One step = one bsa_fp8_prefill call over the whole workload (active-tile compaction, paged
+TMA loads, tcgen05 QK^T and PV, online softmax with e4m3 P, epilogue), inputs resident in HBM.
+The default workload is 2 x 8192-token prefills, 32 query / 8 KV heads, page 64, per-token K
+and per-head V descales, 1% outlier channels, block mask keeping each causal off-diagonal tile
+with probability 0.5 (the diagonal always kept).
+
+Metric: effective TFLOP/s over active tiles, FLOPs = sum over (task, active tile) of
+4 * 128 * rows_valid * cols_valid.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
+Under torchrun every rank runs an independent replica of the workload (weak scaling; the
+path has no data exchange), timed between barriers, max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = ("block-sparse FP8 prefill effective TFLOPS (active tiles) and ms/call, "
+          "% FP8 roofline")
+DEFAULT_WORKLOAD = "prefill_2x8k_h32kv8_bsm50_outliers"
+FP8_PER_BF16 = 2.0        # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.WORKLOAD_ORDER)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
+
+
+def config_of(case, name, tiles, flops):
+    Q = sum(-(-ql // 128) for ql in case.q_lens) * case.N1
+    mask = ("block_mask" if case.block_mask is not None else
+            "sparse_indices" if case.sparse_indices is not None else "dense")
+    return {"workload": name, "B": case.B, "q_lens": case.q_lens, "kv_lens": case.kv_lens,
+            "N1": case.N1, "N2": case.N2, "D": 128, "page_size": case.page_size,
+            "k_scale": ["per_tensor", "per_token_head"][case.k_scale_kind],
+            "v_scale": ["per_tensor", "", "per_head"][case.v_scale_kind],
+            "mask": mask, "causal": bool(case.causal), "tasks": Q,
+            "active_tiles": int(tiles), "effective_gflop": round(flops / 1e9, 3),
+            "l2": "flushed (512 MiB write) before every step, outside the per-step events"}
+
+
+def cpu_info():
+    import oracle
+
+    return oracle.cpu_model(), os.cpu_count()
+
+
+def cpu_baseline(case, lists, counts, seconds, seed=11):
+    """The oracle (exact fp64 mode, all host threads) on a bounded sample of whole tasks."""
+    import oracle
+
+    orc = oracle.Oracle(case)
+    threads = orc.lib.oracle_max_threads()
+    tasks = [(b, h, qt) for b in range(case.B) for h in range(case.N1)
+             for qt in range(-(-case.q_lens[b] // 128))]
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(len(tasks))
+    done_flops, done_tasks, done_rows, t_total = 0, 0, 0, 0.0
+    i = 0
+    while t_total < seconds and i < len(order):
+        chunk = [tasks[j] for j in order[i:i + 8]]
+        i += 8
+        rows, fl = [], 0
+        for b, h, qt in chunk:
+            q0, ql, kl = int(case.cu_seqlens_q[b]), case.q_lens[b], case.kv_lens[b]
+            nr = min(128, ql - qt * 128)
+            rows += [(q0 + qt * 128 + r, h) for r in range(nr)]
+            ts = lists[b, h, qt, :counts[b, h, qt]].astype(np.int64)
+            fl += 4 * 128 * nr * int(np.minimum(128, kl - ts * 128).sum())
+        t0 = time.perf_counter()
+        orc.rows(np.array(rows, dtype=np.int32), oracle.EXACT)
+        t_total += time.perf_counter() - t0
+        done_flops += fl
+        done_tasks += len(chunk)
+        done_rows += len(rows)
+    model, _ = cpu_info()
+    return {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{done_tasks} of {len(tasks)} (b, h, q-tile) tasks ({done_rows} rows), "
+                      f"seeded random, exact fp64 mode, {t_total:.1f} s on {threads} threads "
+                      f"({model})"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if self.bus_id:
+            cmd += ["-i", self.bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import block_sparse_fp8_gb300 as bsa
+    from block_sparse_fp8_gb300 import _build
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    if _build.needs_build():
+        if rank == 0:
+            _build.build()
+        if world > 1:
+            torch.distributed.barrier()
+    bsa.lib()
+
+    case = W.make_workload(args.workload)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    d = dict(q=t(case.q), k_pages=t(case.k_pages), v_pages=t(case.v_pages),
+             q_descale=t(case.q_descale), k_descale=t(case.k_descale),
+             v_descale=t(case.v_descale), cu_seqlens_q=t(case.cu_seqlens_q),
+             seqused_kv=t(case.seqused_kv), block_table=t(case.block_table),
+             block_mask=t(case.block_mask), sparse_indices=t(case.sparse_indices),
+             sparse_seq_len=t(case.sparse_seq_len))
+    dims = bsa.Dims(**case.dims())
+    lists, counts = bsa.compact_tiles(d["cu_seqlens_q"], d["seqused_kv"], dims,
+                                      block_mask=d["block_mask"],
+                                      sparse_indices=d["sparse_indices"],
+                                      sparse_seq_len=d["sparse_seq_len"])
+    lists, counts = lists.cpu().numpy(), counts.cpu().numpy()
+    tiles, flops = W.active_work(case, (lists, counts))
+
+    out = torch.empty((case.T, case.N1, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((case.N1, case.T), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        bsa.prefill(d["q"], d["k_pages"], d["v_pages"], d["q_descale"], d["k_descale"],
+                    d["v_descale"], d["cu_seqlens_q"], d["seqused_kv"], d["block_table"],
+                    case.max_q_len, case.max_kv_len, block_mask=d["block_mask"],
+                    sparse_indices=d["sparse_indices"], sparse_seq_len=d["sparse_seq_len"],
+                    softmax_scale=case.softmax_scale, p_scale=case.p_scale,
+                    causal=bool(case.causal), out=out, lse=lse, dev_status=status,
+                    stream=stream, k_scale_kind=case.k_scale_kind,
+                    v_scale_kind=case.v_scale_kind)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+
+    sampler = None
+    if rank == 0 and not args.no_clocks:
+        bus = None
+        try:
+            p = torch.cuda.get_device_properties(dev)
+            bus = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+        except AttributeError:
+            bus = None
+        sampler = ClockSampler(bus)
+        sampler.start()
+        time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(per) / len(per)
+    if world > 1:
+        tt = torch.tensor([ms, wall], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms, wall = float(tt[0]), float(tt[1])
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the timed region")
+
+    # end to end through the public API: host (pinned) inputs in, host output back, per step
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: (None if v is None else v.cpu().pin_memory()) for k, v in d.items()}
+        dev_in = {k: (None if v is None else torch.empty_like(v)) for k, v in d.items()}
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
+        d2h = host_out.numel() * 2 + host_lse.numel() * 4
+        n_e2e = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            for k, v in host_in.items():
+                if v is not None:
+                    dev_in[k].copy_(v, non_blocking=True)
+            bsa.prefill(dev_in["q"], dev_in["k_pages"], dev_in["v_pages"], dev_in["q_descale"],
+                        dev_in["k_descale"], dev_in["v_descale"], dev_in["cu_seqlens_q"],
+                        dev_in["seqused_kv"], dev_in["block_table"], case.max_q_len,
+                        case.max_kv_len, block_mask=dev_in["block_mask"],
+                        sparse_indices=dev_in["sparse_indices"],
+                        sparse_seq_len=dev_in["sparse_seq_len"],
+                        softmax_scale=case.softmax_scale, p_scale=case.p_scale,
+                        causal=bool(case.causal), out=out, lse=lse, stream=stream,
+                        k_scale_kind=case.k_scale_kind, v_scale_kind=case.v_scale_kind)
+            host_out.copy_(out, non_blocking=True)
+            host_lse.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = ev0.elapsed_time(ev1) / n_e2e
+        if world > 1:
+            tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(tt[0])
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        return None
+    pk, src = peaks()
+    fp8_peak = pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS) * FP8_PER_BF16
+    achieved = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic (seeded)",
+        "config": config_of(case, args.workload, tiles, flops),
+        "ms_per_call": {"mean": ms, "median": statistics.median(per), "min": min(per)},
+        "wall_ms_per_step_incl_flush": wall * 1e3 / args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": None,
+                     "peak_source": f"{src}: bf16 {'burst' if src == 'measured' else ''} "
+                                    f"{pk.get('bf16_tflops')} TFLOP/s x {FP8_PER_BF16} "
+                                    f"(nominal fp8/bf16 ratio)",
+                     "kernel": "bsa_attention_kernel"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        line["cpu_baseline"] = cpu_baseline(case, lists, counts, args.cpu_seconds)
+    return line
+
+
+def run_reference(args, rank):
+    """The CPU oracle, as it stands, on the host cores: each step a bounded sample of tasks."""
+    if rank != 0:
+        return None
+    import oracle
+
+    case = W.make_workload(args.workload)
+    orc = oracle.Oracle(case)
+    lists, counts, _err = orc.lists()
+    tiles, flops = W.active_work(case, (lists, counts))
+    tasks = [(b, h, qt) for b in range(case.B) for h in range(case.N1)
+             for qt in range(-(-case.q_lens[b] // 128))]
+    rng = np.random.default_rng(5)
+    per_step_tasks = 4
+    threads = orc.lib.oracle_max_threads()
+
+    def step(i):
+        sel = rng.choice(len(tasks), per_step_tasks, replace=False)
+        rows, fl = [], 0
+        for j in sel:
+            b, h, qt = tasks[j]
+            q0, ql, kl = int(case.cu_seqlens_q[b]), case.q_lens[b], case.kv_lens[b]
+            nr = min(128, ql - qt * 128)
+            rows += [(q0 + qt * 128 + r, h) for r in range(nr)]
+            ts = lists[b, h, qt, :counts[b, h, qt]].astype(np.int64)
+            fl += 4 * 128 * nr * int(np.minimum(128, kl - ts * 128).sum())
+        t0 = time.perf_counter()
+        orc.rows(np.array(rows, dtype=np.int32), oracle.EXACT)
+        return fl, time.perf_counter() - t0
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    tot_f, tot_t = 0, 0.0
+    for i in range(args.steps):
+        f, dt = step(i)
+        tot_f += f
+        tot_t += dt
+    value = tot_f / tot_t / 1e12
+    model, _ = cpu_info()
+    sample = (f"{per_step_tasks} seeded random (b, h, q-tile) tasks per step of {len(tasks)}, "
+              f"exact fp64 mode, {threads} threads ({model})")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": tot_t * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": config_of(case, args.workload, tiles, flops),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        line = run_ours(args, rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if args.impl == "ours" and world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+"""Block-sparse FP8 attention prefill over a paged KV cache on GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in include/bsa_fp8.h: it marshals PyTorch CUDA tensors
+(device pointers) and the current stream into ``bsa_fp8_prefill`` / ``bsa_fp8_compact_tiles``.
+Every step of the computation runs in the library's CUDA kernels; there is no CPU path.
+The library must have been built (``block_sparse_fp8_gb300._build.build()``); importing the
+binding on a machine without it raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import _build
+
+__all__ = ["Dims", "prefill", "compact_tiles", "workspace_size", "status_string", "lib",
+           "SCALE_PER_TENSOR", "SCALE_PER_TOKEN_HEAD", "SCALE_PER_HEAD", "BsaError",
+           "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_BAD_SEQLEN", "DEV_TIMEOUT"]
+
+SCALE_PER_TENSOR = 0
+SCALE_PER_TOKEN_HEAD = 1
+SCALE_PER_HEAD = 2
+
+DEV_BAD_INDEX = 1
+DEV_BAD_PAGE = 2
+DEV_BAD_SEQLEN = 4
+DEV_TIMEOUT = 8
+
+EXPORTED = ("bsa_fp8_prefill", "bsa_fp8_prefill_workspace_size", "bsa_fp8_compact_tiles",
+            "bsa_status_string")
+
+
+class BsaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "B", "N1", "N2", "D", "page_size", "max_q_len", "max_kv_len", "num_pages",
+        "max_pages_per_seq", "total_q", "k_scale_kind", "v_scale_kind", "causal")]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libbsa_fp8.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise ImportError(
+                f"{_build.LIB} is missing: build it with block_sparse_fp8_gb300._build.build()")
+        L = ctypes.CDLL(_build.LIB)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.bsa_fp8_prefill.restype = i32
+        L.bsa_fp8_prefill.argtypes = [ctypes.POINTER(Dims)] + [vp] * 12 + [f32, f32, vp, vp, vp,
+                                                                           sz, vp, vp]
+        L.bsa_fp8_prefill_workspace_size.restype = sz
+        L.bsa_fp8_prefill_workspace_size.argtypes = [ctypes.POINTER(Dims)]
+        L.bsa_fp8_compact_tiles.restype = i32
+        L.bsa_fp8_compact_tiles.argtypes = [ctypes.POINTER(Dims)] + [vp] * 9
+        L.bsa_status_string.restype = ctypes.c_char_p
+        L.bsa_status_string.argtypes = [i32]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().bsa_status_string(status).decode()
+
+
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream):
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def make_dims(q, k_pages, block_table, cu_seqlens_q, max_q_len, max_kv_len, k_scale_kind,
+              v_scale_kind, causal=True) -> Dims:
+    T, N1, D = q.shape
+    P, N2, ps, D2 = k_pages.shape
+    return Dims(B=cu_seqlens_q.shape[0] - 1, N1=N1, N2=N2, D=D, page_size=ps,
+                max_q_len=int(max_q_len), max_kv_len=int(max_kv_len), num_pages=P,
+                max_pages_per_seq=block_table.shape[1], total_q=T,
+                k_scale_kind=int(k_scale_kind), v_scale_kind=int(v_scale_kind),
+                causal=int(bool(causal)))
+
+
+def workspace_size(dims: Dims) -> int:
+    return int(lib().bsa_fp8_prefill_workspace_size(ctypes.byref(dims)))
+
+
+def prefill(q, k_pages, v_pages, q_descale, k_descale, v_descale, cu_seqlens_q, seqused_kv,
+            block_table, max_q_len: int, max_kv_len: int, block_mask=None, sparse_indices=None,
+            sparse_seq_len=None, softmax_scale: float | None = None, p_scale: float = 256.0,
+            causal: bool = True, out=None, lse=None, return_lse: bool = True, dev_status=None,
+            workspace=None, stream=None, k_scale_kind: int | None = None,
+            v_scale_kind: int | None = None):
+    """Block-sparse FP8 prefill.  Tensors are CUDA tensors in the C ABI's layouts:
+    q uint8/float8_e4m3fn [T, N1, 128]; k_pages, v_pages [P, N2, page, 128]; q_descale f32
+    [T, N1]; k_descale f32 [1] or [P, N2, page]; v_descale f32 [1] or [N2]; cu_seqlens_q i32
+    [B+1]; seqused_kv i32 [B] or None; block_table i32 [B, L]; block_mask u8 [B, N1, Qb, Kb]
+    or sparse_indices i32 [B, N1, Qb, Kb] + sparse_seq_len i32 [B, N1, Qb].
+    max_q_len / max_kv_len are host integers (upper bounds of the per-sequence lengths).
+    The scale kinds default to what the descale shapes imply (K [P, N2, page] = per token and
+    head; V [N2] = per head, which for N2 = 1 is the same as per tensor).
+    Returns (out bf16 [T, N1, 128], lse f32 [N1, T] or None)."""
+    import torch
+
+    k_kind = k_scale_kind if k_scale_kind is not None else (
+        SCALE_PER_TOKEN_HEAD if k_descale.dim() == 3 else SCALE_PER_TENSOR)
+    v_kind = v_scale_kind if v_scale_kind is not None else (
+        SCALE_PER_HEAD if v_descale.numel() == k_pages.shape[1] else SCALE_PER_TENSOR)
+    dims = make_dims(q, k_pages, block_table, cu_seqlens_q, max_q_len, max_kv_len, k_kind,
+                     v_kind, causal)
+    T, N1, D = q.shape
+    if out is None:
+        out = torch.empty((T, N1, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((N1, T), dtype=torch.float32, device=q.device)
+    ws_bytes = workspace_size(dims)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    st = lib().bsa_fp8_prefill(
+        ctypes.byref(dims), _p(q), _p(k_pages), _p(v_pages), _p(q_descale), _p(k_descale),
+        _p(v_descale), _p(cu_seqlens_q), _p(seqused_kv), _p(block_table), _p(block_mask),
+        _p(sparse_indices), _p(sparse_seq_len), float(softmax_scale), float(p_scale), _p(out),
+        _p(lse), _p(workspace), ws_bytes, _p(dev_status), _stream_handle(stream))
+    if st != 0:
+        raise BsaError(st, "bsa_fp8_prefill")
+    return out, lse
+
+
+def compact_tiles(cu_seqlens_q, seqused_kv, dims: Dims, block_mask=None, sparse_indices=None,
+                  sparse_seq_len=None, dev_status=None, stream=None):
+    """Active-tile lists [B, N1, Qb, Kb] (-1 past the count) and counts [B, N1, Qb]."""
+    import torch
+
+    Qb = -(-dims.max_q_len // 128)
+    Kb = -(-dims.max_kv_len // 128)
+    dev = cu_seqlens_q.device
+    lists = torch.empty((dims.B, dims.N1, Qb, Kb), dtype=torch.int32, device=dev)
+    counts = torch.empty((dims.B, dims.N1, Qb), dtype=torch.int32, device=dev)
+    st = lib().bsa_fp8_compact_tiles(ctypes.byref(dims), _p(cu_seqlens_q), _p(seqused_kv),
+                                     _p(block_mask), _p(sparse_indices), _p(sparse_seq_len),
+                                     _p(lists), _p(counts), _p(dev_status),
+                                     _stream_handle(stream))
+    if st != 0:
+        raise BsaError(st, "bsa_fp8_compact_tiles")
+    return lists, counts

@@ -1,0 +1,156 @@
+/*
+ * bsa_fp8.h -- C ABI of the block-sparse FP8 attention prefill library for GB300 (sm_103a).
+ *
+ * What it computes (Quant Block Sparse Attention, CANNBotDSL sample, section 算子介绍):
+ *
+ *   Q^_i = Q_i^fp8 * q_descale_i,   K^_j = K_j^fp8 * k_descale_j,   V^_j = V_j^fp8 * v_descale_head(j)
+ *   O_i  = sum_{j in A_i} softmax_{j in A_i}( Q^_i . K^_j * softmax_scale ) V^_j
+ *   LSE_i = ln sum_{j in A_i} exp( Q^_i . K^_j * softmax_scale )
+ *
+ * where A_i is the set of keys j of the same sequence that
+ *   (1) lie in a 128-token KV tile enabled for the 128-token Q tile of row i -- by a uint8
+ *       block_mask (hpc-ops Block-Sparse FP8 Attention, section 块稀疏调度), by a
+ *       sparse_indices / sparse_seq_len list (Quant Block Sparse Attention, section
+ *       稀疏索引与 PA 页表), or all tiles when neither is given (the dense path);
+ *   (2) satisfy j < kv_len (the tail block's padding never takes part);
+ *   (3) when causal, satisfy j <= i + (kv_len - q_len)  (right-context causal).
+ * A row with an empty A_i gets O_i = 0 and LSE_i = -FLT_MAX.
+ *
+ * The probabilities are quantised to e4m3 at a fixed scale p_scale (256 by default) before
+ * the P.V product and the scale is undone in the epilogue together with the V descale
+ * (hpc-ops Block-Sparse FP8 Attention, section 固定 P-scale 量化技巧).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device unless stated.
+ *   - The caller owns every buffer.  The library never allocates, frees or synchronises;
+ *     all work is queued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *   - Validation reads only `dims`, scalars and pointer values (null / alignment).  The host
+ *     never reads device memory (Quant Block Sparse Attention, section 算子介绍: the host only
+ *     checks static parameters and launches asynchronously).
+ *   - Errors in device data (a sparse index outside [0, Kb), a sparse_seq_len outside
+ *     [0, Kb], a block_table entry outside [0, num_pages) for a needed page, a sequence
+ *     length outside its declared maximum) are reported by OR-ing BSA_DEV_* bits into
+ *     *dev_status (if dev_status is not NULL) -- read it after synchronising.  The bad
+ *     entry is skipped (a bad page reads as zeros); nothing traps or hangs.
+ *   - Every wait inside the kernels is bounded; a wait that runs out sets BSA_DEV_TIMEOUT.
+ */
+#ifndef BSA_FP8_H
+#define BSA_FP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BSA_OK = 0,
+  BSA_ERR_INVALID_ARGUMENT = 1, /* bad dims, scalar, null or misaligned pointer */
+  BSA_ERR_UNSUPPORTED = 2,      /* valid but outside what this build supports (GPU arch, Kb) */
+  BSA_ERR_CUDA = 3,             /* a CUDA call or kernel launch failed */
+  BSA_ERR_WORKSPACE = 4         /* workspace smaller than bsa_fp8_prefill_workspace_size() */
+} bsa_status_t;
+
+/* Quantisation granularity of K and V (hpc-ops article, QuantType list):
+ *   QPERTOKEN_PERHEAD_KPERTENSOR_VPERTENSOR      -> k: PER_TENSOR,     v: PER_TENSOR
+ *   QPERTOKEN_PERHEAD_KPERTOKEN_PERHEAD_VPERHEAD -> k: PER_TOKEN_HEAD, v: PER_HEAD
+ * Q is always per token per head. */
+typedef enum {
+  BSA_SCALE_PER_TENSOR = 0,     /* one fp32 scalar, k_descale[0] / v_descale[0] */
+  BSA_SCALE_PER_TOKEN_HEAD = 1, /* K only: fp32 [num_pages, N2, page_size] */
+  BSA_SCALE_PER_HEAD = 2        /* V only: fp32 [N2] */
+} bsa_scale_kind_t;
+
+/* bits OR-ed into *dev_status */
+#define BSA_DEV_BAD_INDEX 1   /* sparse index or sparse_seq_len out of range (entry skipped) */
+#define BSA_DEV_BAD_PAGE 2    /* block_table entry out of range for a needed page (reads 0) */
+#define BSA_DEV_BAD_SEQLEN 4  /* q_len / kv_len negative or above the declared maximum */
+#define BSA_DEV_TIMEOUT 8     /* a bounded wait inside a kernel ran out */
+
+/* Problem geometry (host struct).  Layouts follow the Quant Block Sparse Attention
+ * parameter table with the page size made a parameter:
+ *   q            e4m3 [total_q, N1, 128]            (TND; row of token t, head h at (t*N1+h)*128)
+ *   k/v pages    e4m3 [num_pages, N2, page_size, 128]
+ *   block_table  int32 [B, max_pages_per_seq]; logical page l of sequence b -> physical page
+ * Q tile = KV tile = 128 tokens; Qb = ceil(max_q_len/128), Kb = ceil(max_kv_len/128).
+ * The KV head of query head h is h / (N1/N2). */
+typedef struct {
+  int B;                 /* sequences, >= 0 */
+  int N1;                /* query heads, >= 1 */
+  int N2;                /* KV heads, N1 % N2 == 0, 1 <= N1/N2 <= 16 */
+  int D;                 /* head dim, must be 128 */
+  int page_size;         /* tokens per KV page: 32 or 64 */
+  int max_q_len;         /* >= every q_len (sets Qb) */
+  int max_kv_len;        /* >= every kv_len (sets Kb); Kb <= 4096 */
+  int num_pages;         /* physical pages in k/v pages */
+  int max_pages_per_seq; /* L, columns of block_table; L * page_size >= max_kv_len */
+  int total_q;           /* T = cu_seqlens_q[B] */
+  int k_scale_kind;      /* BSA_SCALE_PER_TENSOR or BSA_SCALE_PER_TOKEN_HEAD */
+  int v_scale_kind;      /* BSA_SCALE_PER_TENSOR or BSA_SCALE_PER_HEAD */
+  int causal;            /* 1 = right-context causal (mask_mode 3), 0 = no causal mask (mode 0) */
+} bsa_fp8_dims_t;
+
+/* Bytes of device workspace bsa_fp8_prefill needs for `dims` (0 = none; then `workspace`
+ * may be NULL).  Returns 0 for invalid dims as well; bsa_fp8_prefill reports those. */
+size_t bsa_fp8_prefill_workspace_size(const bsa_fp8_dims_t *dims);
+
+/* Block-sparse FP8 attention prefill over a paged KV cache.
+ *
+ *   q               e4m3 [T, N1, 128], 16-byte aligned
+ *   k_pages,v_pages e4m3 [num_pages, N2, page_size, 128], 16-byte aligned; slots past a
+ *                   sequence's kv_len in its last page must hold zeros (hpc-ops article,
+ *                   快速上手: unused slots are zero-filled)
+ *   q_descale       fp32 [T, N1]
+ *   k_descale       fp32 [1] (PER_TENSOR) or [num_pages, N2, page_size] (PER_TOKEN_HEAD,
+ *                   16-byte aligned)
+ *   v_descale       fp32 [1] (PER_TENSOR) or [N2] (PER_HEAD)
+ *   cu_seqlens_q    int32 [B+1], cu_seqlens_q[0] = 0, non-decreasing, cu_seqlens_q[B] = T
+ *   seqused_kv      int32 [B] KV tokens per sequence, or NULL (then kv_len = q_len)
+ *   block_table     int32 [B, max_pages_per_seq]
+ *   block_mask      uint8 [B, N1, Qb, Kb], nonzero = compute; or NULL
+ *   sparse_indices  int32 [B, N1, Qb, Kb] logical KV tiles per Q tile (any order; only the
+ *                   first sparse_seq_len[b,h,qt] entries are read; repeats count once); or NULL
+ *   sparse_seq_len  int32 [B, N1, Qb]; required with sparse_indices
+ *                   At most one of block_mask / sparse_indices; neither = dense path.
+ *   softmax_scale   finite (usually 1/sqrt(128))
+ *   p_scale         fixed P-scale; <= 0 selects the default 256; must be finite
+ *   out_bf16        bf16 [T, N1, 128] (written)
+ *   lse_f32         fp32 [N1, T] natural-log LSE (written), or NULL
+ *   workspace       device buffer of bsa_fp8_prefill_workspace_size(dims) bytes (may be NULL
+ *                   when that is 0)
+ *   dev_status      device int, OR-ed with BSA_DEV_* bits on data errors; or NULL
+ *   stream          cudaStream_t
+ */
+bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *q, const void *k_pages,
+                             const void *v_pages, const float *q_descale, const float *k_descale,
+                             const float *v_descale, const int *cu_seqlens_q,
+                             const int *seqused_kv, const int *block_table,
+                             const uint8_t *block_mask, const int *sparse_indices,
+                             const int *sparse_seq_len, float softmax_scale, float p_scale,
+                             void *out_bf16, float *lse_f32, void *workspace,
+                             size_t workspace_bytes, int *dev_status, void *stream);
+
+/* The active-tile lists the prefill kernel computes, written out so they can be compared
+ * bit-exactly (hpc-ops article, section 活跃 tile 列表: a warp ballot writes the active KV
+ * tiles of a Q tile in order).  For task (b, h, qt):
+ *   tile_lists [B, N1, Qb, Kb] int32: the enabled tiles t < kend(b, qt), ascending, without
+ *                                     repeats, then -1 up to Kb
+ *   tile_counts [B, N1, Qb] int32:   their number (0 for qt >= ceil(q_len_b/128))
+ * kend(b, qt) is the first KV tile no row of the Q tile can see: ceil(min(kv_len,
+ * last_row + kv_len - q_len + 1) / 128) when causal, ceil(kv_len / 128) otherwise.
+ * Same argument rules and error reporting as bsa_fp8_prefill. */
+bsa_status_t bsa_fp8_compact_tiles(const bsa_fp8_dims_t *dims, const int *cu_seqlens_q,
+                                   const int *seqused_kv, const uint8_t *block_mask,
+                                   const int *sparse_indices, const int *sparse_seq_len,
+                                   int *tile_lists, int *tile_counts, int *dev_status,
+                                   void *stream);
+
+/* Static text for a status code. */
+const char *bsa_status_string(bsa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_FP8_H */

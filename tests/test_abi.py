@@ -1,0 +1,114 @@
+"""The C-ABI library loads, exports every symbol include/bsa_fp8.h declares, and validates its
+arguments on the host (no GPU needed: every call here returns before touching CUDA)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+import block_sparse_fp8_gb300 as bsa
+from block_sparse_fp8_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "bsa_fp8.h")
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.fixture(scope="module")
+def L():
+    if _build.needs_build():
+        if shutil.which(_build.nvcc()) is None and not os.path.exists(_build.nvcc()):
+            pytest.skip("nvcc not available")
+        _build.build()
+    return bsa.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsa_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_set():
+    assert declared_functions() == sorted(bsa.EXPORTED)
+
+
+def test_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code in range(5):
+        assert bsa.status_string(code)
+    assert "unknown" in bsa.status_string(99)
+
+
+def _dims(**kw):
+    base = dict(B=1, N1=8, N2=1, D=128, page_size=64, max_q_len=1024, max_kv_len=1024,
+                num_pages=16, max_pages_per_seq=16, total_q=1024, k_scale_kind=0,
+                v_scale_kind=0, causal=1)
+    base.update(kw)
+    return bsa.Dims(**base)
+
+
+def _prefill(L, dims, **ptrs):
+    fake = 0x10000  # never dereferenced: every case below fails validation first
+    args = dict(q=fake, k=fake, v=fake, qd=fake, kd=fake, vd=fake, cu=fake, su=fake, bt=fake,
+                mask=None, idx=None, sl=None, scale=0.088, pscale=256.0, out=fake, lse=fake)
+    args.update(ptrs)
+    return L.bsa_fp8_prefill(ctypes.byref(dims), args["q"], args["k"], args["v"], args["qd"],
+                             args["kd"], args["vd"], args["cu"], args["su"], args["bt"],
+                             args["mask"], args["idx"], args["sl"], args["scale"],
+                             args["pscale"], args["out"], args["lse"], None, 0, None, None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(D=64), dict(page_size=48), dict(page_size=128), dict(N1=6, N2=4), dict(N1=34, N2=2),
+    dict(N1=0), dict(N2=0), dict(max_q_len=-1), dict(max_kv_len=-5), dict(total_q=-1),
+    dict(max_pages_per_seq=15), dict(k_scale_kind=2), dict(v_scale_kind=1),
+    dict(causal=2), dict(B=-1)])
+def test_invalid_dims(L, bad):
+    assert _prefill(L, _dims(**bad)) == INVALID
+
+
+def test_too_many_kv_tiles_unsupported(L):
+    d = _dims(max_kv_len=4097 * 128, max_pages_per_seq=4097 * 2, num_pages=8194 * 1)
+    assert _prefill(L, d) == UNSUPPORTED
+
+
+def test_invalid_scalars_and_pointers(L):
+    d = _dims()
+    assert _prefill(L, d, scale=float("inf")) == INVALID
+    assert _prefill(L, d, scale=float("nan")) == INVALID
+    assert _prefill(L, d, pscale=float("nan")) == INVALID
+    assert _prefill(L, d, pscale=float("inf")) == INVALID
+    assert _prefill(L, d, mask=0x20000, idx=0x30000, sl=0x40000) == INVALID   # both forms
+    assert _prefill(L, d, idx=0x30000) == INVALID                              # no seq_len
+    for k in ("q", "k", "v", "qd", "kd", "vd", "cu", "bt", "out"):
+        assert _prefill(L, d, **{k: None}) == INVALID, k
+    assert _prefill(L, d, q=0x10001) == INVALID     # TMA needs 16-byte aligned bases
+    assert _prefill(L, d, k=0x10008) == INVALID
+    assert _prefill(L, _dims(num_pages=0)) == INVALID
+
+
+def test_empty_problem_is_a_no_op(L):
+    assert _prefill(L, _dims(B=0, total_q=0)) == 0
+    assert _prefill(L, _dims(total_q=0)) == 0
+    assert _prefill(L, _dims(max_q_len=0, total_q=0)) == 0
+
+
+def test_compact_validation(L):
+    d = _dims(page_size=16)
+    assert L.bsa_fp8_compact_tiles(ctypes.byref(d), 1, None, None, None, None, 1, 1, None,
+                                   None) == INVALID
+    d = _dims()
+    assert L.bsa_fp8_compact_tiles(ctypes.byref(d), 0x100, None, 0x200, 0x300, 0x400, 0x500,
+                                   0x600, None, None) == INVALID
+
+
+def test_workspace_query(L):
+    assert bsa.workspace_size(_dims()) == 0

@@ -1,0 +1,235 @@
+"""The CUDA path against the CPU oracle, element by element (needs a GB300)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from gpu_helpers import (EXACT_ATOL, EXACT_RTOL, NEG_FLT_MAX, PEMU_ATOL, PEMU_RTOL, check_lse,
+                         check_o, ensure_built, run, run_lists, sample_rows, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+SMALL = {
+    # several Q and KV tiles, ragged tails, GQA, both scale kinds, both page sizes
+    "bern_ragged": dict(seed=101, q_lens=[300, 129, 1], kv_lens=[300, 129, 1], N1=4, N2=2,
+                        page_size=64, k_scale_kind=1, v_scale_kind=2, mask="bernoulli"),
+    "bern_pt_p32": dict(seed=102, q_lens=[640], kv_lens=[640], N1=8, N2=1, page_size=32,
+                        mask="bernoulli", keep=0.5),
+    "chunked_off": dict(seed=103, q_lens=[200, 130], kv_lens=[900, 300], N1=4, N2=1,
+                        page_size=64, k_scale_kind=1, v_scale_kind=2, mask="local_sink",
+                        n_local=1, p_far=0.3),
+    "indices_empty": dict(seed=104, q_lens=[520, 260, 77], kv_lens=[520, 260, 77], N1=4, N2=2,
+                          page_size=32, k_scale_kind=1, v_scale_kind=2, mask="indices",
+                          sparse_frac=0.5, n_empty=3),
+    "dense_none": dict(seed=105, q_lens=[383], kv_lens=[383], N1=2, N2=2, page_size=64,
+                       mask="none"),
+    "q_longer_than_kv": dict(seed=106, q_lens=[300], kv_lens=[170], N1=2, N2=1, page_size=64,
+                             mask="ones"),
+    "noncausal": dict(seed=107, q_lens=[200, 140], kv_lens=[330, 140], N1=4, N2=2,
+                      page_size=32, k_scale_kind=1, v_scale_kind=2, mask="ones", causal=0),
+    "gqa16": dict(seed=108, q_lens=[260], kv_lens=[260], N1=16, N2=1, page_size=64,
+                  k_scale_kind=1, v_scale_kind=2, mask="bernoulli"),
+    "pscale_odd": dict(seed=109, q_lens=[256], kv_lens=[256], N1=2, N2=1, page_size=64,
+                       mask="bernoulli", p_scale=100.5),
+    "outliers": dict(seed=110, q_lens=[512], kv_lens=[512], N1=4, N2=2, page_size=64,
+                     k_scale_kind=1, v_scale_kind=2, mask="bernoulli", outlier_frac=0.05),
+    "long_kv_many_tiles": dict(seed=111, q_lens=[128], kv_lens=[3000], N1=2, N2=1,
+                               page_size=32, k_scale_kind=1, v_scale_kind=2, mask="ones"),
+}
+
+
+def _case(name):
+    kw = dict(SMALL[name])
+    return W.make_case(name, **kw)
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_lists_bit_exact(name):
+    case = _case(name)
+    ref_l, ref_c, ref_err = O.Oracle(case).lists()
+    lists, counts, st = run_lists(case)
+    assert st == 0 and ref_err == 0
+    assert np.array_equal(counts, ref_c)
+    assert np.array_equal(lists, ref_l)
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_attention_all_rows(name):
+    case = _case(name)
+    orc = O.Oracle(case)
+    out, lse, st = run(case)
+    assert st == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    gl = lse.cpu().numpy().astype(np.float64)
+    o_ex, l_ex, _ = orc.all_rows(O.EXACT)
+    o_pe, l_pe, _ = orc.all_rows(O.PEMU)
+    check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, f"{name} vs exact")
+    check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, f"{name} vs P-emulating")
+    check_lse(gl, l_ex, f"{name} lse")
+    # empty rows exactly 0 / -FLT_MAX
+    empty = l_ex == NEG_FLT_MAX
+    assert np.all(gl[empty] == np.float32(NEG_FLT_MAX))
+    assert not got.transpose(1, 0, 2)[empty].any()
+
+
+def test_empty_tasks_exact_zero():
+    case = _case("indices_empty")
+    out, lse, _ = run(case)
+    got, gl = out.float().cpu().numpy(), lse.cpu().numpy()
+    n = 0
+    for b in range(case.B):
+        q0 = int(case.cu_seqlens_q[b])
+        for h in range(case.N1):
+            for qt in range(-(-case.q_lens[b] // 128)):
+                if case.sparse_seq_len[b, h, qt] == 0:
+                    r = slice(q0 + qt * 128, q0 + min(case.q_lens[b], qt * 128 + 128))
+                    assert not got[r, h].any()
+                    assert np.all(gl[h, r] == np.float32(NEG_FLT_MAX))
+                    n += 1
+    assert n == 3
+
+
+def test_ones_mask_equals_dense_bitwise():
+    kw = dict(q_lens=[300, 90], kv_lens=[300, 400], N1=4, N2=2, page_size=64, k_scale_kind=1,
+              v_scale_kind=2)
+    a = W.make_case("a", 120, mask="ones", **kw)
+    b = W.make_case("b", 120, mask="none", **kw)
+    oa, la, _ = run(a)
+    ob, lb, _ = run(b)
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+
+
+def test_indices_equal_mask_bitwise():
+    m = W.make_case("m", 121, [400, 130], [400, 130], 4, 2, 64, mask="bernoulli", keep=0.4)
+    rng = np.random.default_rng(121)
+    idx = np.full(m.block_mask.shape, -1, dtype=np.int32)
+    n = np.zeros(m.block_mask.shape[:3], dtype=np.int32)
+    for key in np.ndindex(*m.block_mask.shape[:3]):
+        on = np.nonzero(m.block_mask[key])[0]
+        rng.shuffle(on)
+        idx[key][:len(on)] = on
+        n[key] = len(on)
+    s = W.make_case("m", 121, [400, 130], [400, 130], 4, 2, 64, mask="none")
+    s.sparse_indices, s.sparse_seq_len = idx, n
+    oa, la, _ = run(m)
+    ob, lb, _ = run(s)
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+
+
+def test_masked_pages_never_read():
+    """Pages of tiles no task of a KV group enables are filled with e4m3 NaN: bitwise same O."""
+    case = W.make_case("poison", 122, [256], [1024], 4, 2, 64, mask="local_sink", n_local=0,
+                       p_far=0.0)
+    oa, la, _ = run(case)
+    used = set()
+    for b in range(case.B):
+        for h in range(case.N1):
+            for qt in range(case.Qb):
+                for t in np.nonzero(case.block_mask[b, h, qt])[0]:
+                    used.add((h // 2, int(t)))
+    for g in range(case.N2):
+        for t in range(case.Kb):
+            if (g, t) not in used:
+                for lp in range(t * 2, t * 2 + 2):
+                    pg = case.block_table[0, lp]
+                    case.k_pages[pg, g] = 0x7F
+                    case.v_pages[pg, g] = 0x7F
+    ob, lb, _ = run(case)
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+
+
+def test_page_permutation_bitwise():
+    kw = dict(q_lens=[300, 77], kv_lens=[300, 500], N1=4, N2=2, page_size=32, k_scale_kind=1,
+              v_scale_kind=2)
+    a = W.make_case("perm", 123, identity_pages=True, **kw)
+    b = W.make_case("perm", 123, identity_pages=False, **kw)
+    oa, la, _ = run(a)
+    ob, lb, _ = run(b)
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+
+
+def test_tail_slots_ignored_bitwise():
+    kw = dict(q_lens=[300, 100], kv_lens=[300, 100], N1=2, N2=1, page_size=64, k_scale_kind=1,
+              v_scale_kind=2, mask="ones")
+    a = W.make_case("t", 124, **kw)
+    b = W.make_case("t", 124, tail_fill=1.0, **kw)
+    oa, la, _ = run(a)
+    ob, lb, _ = run(b)
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+
+
+def test_without_lse_and_seqused():
+    case = W.make_case("nl", 125, [200], [200], 2, 1, 64, mask="bernoulli")
+    d = to_device(case)
+    d["seqused_kv"] = None
+    o1, l1, _ = run(case, d)
+    o2, l2, _ = run(case, d, return_lse=False)
+    assert l2 is None and torch.equal(o1, o2)
+
+
+def test_device_errors_reported():
+    case = W.make_case("bad", 126, [256], [256], 2, 1, 64, mask="indices", sparse_frac=1.0)
+    case.sparse_indices[0, 0, 1, 0] = 99           # outside [0, Kb)
+    _, _, st = run(case)
+    assert st & 1
+    case2 = W.make_case("badpg", 127, [256], [256], 2, 1, 64, mask="ones")
+    case2.block_table[0, 1] = 10_000               # outside [0, num_pages)
+    _, _, st2 = run(case2)
+    assert st2 & 2
+
+
+def test_zero_length_sequences():
+    case = W.make_case("z", 128, [0, 130, 0], [0, 130, 5], 2, 1, 64, mask="bernoulli")
+    orc = O.Oracle(case)
+    out, lse, st = run(case)
+    assert st == 0
+    o_ex, l_ex, _ = orc.all_rows(O.EXACT)
+    check_o(out.float().cpu().numpy(), o_ex, EXACT_ATOL, EXACT_RTOL, "zero-length")
+    check_lse(lse.cpu().numpy(), l_ex, "zero-length")
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", W.WORKLOAD_ORDER)
+def test_workload_parity(name):
+    case = W.make_workload(name)
+    d = to_device(case)
+    ref_l, ref_c, _ = O.Oracle(case).lists()
+    lists, counts, st = run_lists(case, d)
+    assert st == 0
+    assert np.array_equal(counts, ref_c) and np.array_equal(lists, ref_l)
+    out, lse, st = run(case, d)
+    assert st == 0
+    orc = O.Oracle(case)
+    rows = sample_rows(case, 1536 if case.T > 4096 else case.T * case.N1, seed=7)
+    if case.T * case.N1 <= 65536:
+        o_ex, l_ex, _ = orc.all_rows(O.EXACT)
+        o_pe, _, _ = orc.all_rows(O.PEMU)
+        got = out.float().cpu().numpy()
+        gl = lse.cpu().numpy()
+    else:
+        o_ex, l_ex, _ = orc.rows(rows, O.EXACT)
+        o_pe, _, _ = orc.rows(rows, O.PEMU)
+        got = out.float()[rows[:, 0], rows[:, 1]].cpu().numpy()
+        gl = lse[rows[:, 1], rows[:, 0]].cpu().numpy()
+    check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, f"{name} vs exact")
+    check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, f"{name} vs P-emulating")
+    check_lse(gl, l_ex, f"{name} lse")
+    if case.block_mask is None and case.sparse_indices is None:
+        # the dense path equals an all-ones mask bit for bit
+        ones = torch.ones((case.B, case.N1, case.Qb, case.Kb), dtype=torch.uint8, device="cuda")
+        d2 = dict(d, block_mask=ones)
+        o2, l2, _ = run(case, d2)
+        assert torch.equal(out, o2) and torch.equal(lse, l2)
