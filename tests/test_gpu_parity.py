@@ -43,7 +43,7 @@ SMALL = {
     "pscale_odd": dict(seed=109, q_lens=[256], kv_lens=[256], N1=2, N2=1, page_size=64,
                        mask="bernoulli", p_scale=100.5),
     "outliers": dict(seed=110, q_lens=[512], kv_lens=[512], N1=4, N2=2, page_size=64,
-                     k_scale_kind=1, v_scale_kind=2, mask="bernoulli", outlier_frac=0.05),
+                     k_scale_kind=1, v_scale_kind=2, mask="bernoulli", outlier_frac=0.01),
     "long_kv_many_tiles": dict(seed=111, q_lens=[128], kv_lens=[3000], N1=2, N2=1,
                                page_size=32, k_scale_kind=1, v_scale_kind=2, mask="ones"),
 }
@@ -74,13 +74,37 @@ def test_attention_all_rows(name):
     gl = lse.cpu().numpy().astype(np.float64)
     o_ex, l_ex, _ = orc.all_rows(O.EXACT)
     o_pe, l_pe, _ = orc.all_rows(O.PEMU)
-    check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, f"{name} vs exact")
     check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, f"{name} vs P-emulating")
     check_lse(gl, l_ex, f"{name} lse")
+    # vs the exact formula: within the 0.5% allowance, or -- where rounding P to e4m3 at the
+    # fixed scale already costs more than that (few keys per row, odd p_scale) -- no worse
+    # than the P-emulating oracle itself
+    emu_out = np.mean(np.abs(o_pe - o_ex) > EXACT_ATOL + EXACT_RTOL * np.abs(o_ex))
+    gpu_out = np.mean(np.abs(got - o_ex) > EXACT_ATOL + EXACT_RTOL * np.abs(o_ex))
+    assert gpu_out <= max(0.005, emu_out + 0.002), (name, gpu_out, emu_out)
     # empty rows exactly 0 / -FLT_MAX
     empty = l_ex == NEG_FLT_MAX
     assert np.all(gl[empty] == np.float32(NEG_FLT_MAX))
     assert not got.transpose(1, 0, 2)[empty].any()
+
+
+def test_heavy_outliers_follow_the_method():
+    """5% of channels x8: e4m3 rounding of P alone (the P-emulating oracle) already puts
+    ~0.8% of elements outside the exact band.  The kernel must sit in the tight band around
+    the P-emulating oracle, and miss the exact band only where the method itself does."""
+    case = W.make_case("heavy", 110, [512], [512], 4, 2, 64, 1, 2, "bernoulli",
+                       outlier_frac=0.05)
+    orc = O.Oracle(case)
+    out, lse, _ = run(case)
+    got = out.float().cpu().numpy().astype(np.float64)
+    o_ex, l_ex, _ = orc.all_rows(O.EXACT)
+    o_pe, _, _ = orc.all_rows(O.PEMU)
+    check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, "heavy outliers vs P-emulating")
+    check_lse(lse.cpu().numpy(), l_ex, "heavy outliers lse")
+    gpu_out = np.abs(got - o_ex) > EXACT_ATOL + EXACT_RTOL * np.abs(o_ex)
+    emu_out = np.abs(o_pe - o_ex) > EXACT_ATOL + EXACT_RTOL * np.abs(o_ex)
+    assert emu_out.mean() > 0.005                        # the method's own gap
+    assert abs(gpu_out.mean() - emu_out.mean()) < 0.002  # the kernel adds nothing to it
 
 
 def test_empty_tasks_exact_zero():
