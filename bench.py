@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="keep only the first N sequences of the workload (profiling runs)")
     return ap.parse_args()
 
 
@@ -179,6 +181,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def make_workload(args):
+    kw = dict(W.WORKLOADS[args.workload])
+    if args.batch:
+        kw["q_lens"] = kw["q_lens"][:args.batch]
+        kw["kv_lens"] = kw["kv_lens"][:args.batch]
+    return W.make_case(args.workload, **kw)
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -199,7 +209,7 @@ def run_ours(args, rank, world):
             torch.distributed.barrier()
     bsa.lib()
 
-    case = W.make_workload(args.workload)
+    case = make_workload(args)
     t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     d = dict(q=t(case.q), k_pages=t(case.k_pages), v_pages=t(case.v_pages),
              q_descale=t(case.q_descale), k_descale=t(case.k_descale),
@@ -352,7 +362,7 @@ def run_reference(args, rank):
         return None
     import oracle
 
-    case = W.make_workload(args.workload)
+    case = make_workload(args)
     orc = oracle.Oracle(case)
     lists, counts, _err = orc.lists()
     tiles, flops = W.active_work(case, (lists, counts))

@@ -223,6 +223,36 @@ def test_zero_length_sequences():
     check_lse(lse.cpu().numpy(), l_ex, "zero-length")
 
 
+def test_many_tasks_per_cta_with_empties():
+    """More tasks than resident CTAs, with empty tasks scattered through the task stream, so
+    every persistent CTA runs several tasks back to back across its double-buffered slots."""
+    case = W.make_case("multi", 130, [2000, 1500, 700, 130], [2000, 1500, 700, 300], 32, 8, 32,
+                       1, 2, "indices", sparse_frac=0.3, n_empty=40)
+    orc = O.Oracle(case)
+    out, lse, st = run(case)
+    assert st == 0
+    rows = sample_rows(case, 6144, seed=130)
+    o_ex, l_ex, _ = orc.rows(rows, O.EXACT)
+    o_pe, _, _ = orc.rows(rows, O.PEMU)
+    got = out.float()[rows[:, 0], rows[:, 1]].cpu().numpy()
+    gl = lse[rows[:, 1], rows[:, 0]].cpu().numpy()
+    check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, "multi vs exact")
+    check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, "multi vs P-emulating")
+    check_lse(gl, l_ex, "multi lse")
+    full = out.float().cpu().numpy()
+    fl = lse.cpu().numpy()
+    n = 0
+    for b in range(case.B):
+        q0 = int(case.cu_seqlens_q[b])
+        for h in range(case.N1):
+            for qt in range(-(-case.q_lens[b] // 128)):
+                if case.sparse_seq_len[b, h, qt] == 0:
+                    r = slice(q0 + qt * 128, q0 + min(case.q_lens[b], qt * 128 + 128))
+                    assert not full[r, h].any() and np.all(fl[h, r] == np.float32(NEG_FLT_MAX))
+                    n += 1
+    assert n == 40
+
+
 # ------------------------------------------------------------------ full-size workloads
 
 @pytest.mark.slow
