@@ -112,6 +112,17 @@ static bsa_status_t check_device(size_t attn_smem, int *num_sms) {
       return BSA_ERR_CUDA;
     di.state = (major == 10 && minor == 3) ? 1 : 2;
     di.num_sms = sms;
+    if (di.state == 1) {
+      // The softmax warpgroup raises its registers with setmaxnreg.inc, drawing on what the
+      // CTA was launched with; that only completes if the launch allocation covers the
+      // whole split, so refuse to launch a build where it does not.
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, attn::bsa_attention_kernel) != cudaSuccess)
+        return BSA_ERR_CUDA;
+      if (fa.numRegs * attn::NTHREADS <
+          4 * 32 * attn::CTRL_REGS + 4 * 32 * attn::SOFTMAX_REGS)
+        di.state = 2;
+    }
   }
   if (di.state != 1) return BSA_ERR_UNSUPPORTED;
   if (attn_smem > di.smem_attr) {
