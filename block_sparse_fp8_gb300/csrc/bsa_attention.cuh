@@ -21,6 +21,8 @@
 // formula of Quant Block Sparse Attention (算子介绍).
 #pragma once
 
+#include <type_traits>
+
 #include "bsa_common.cuh"
 #include "ptx_sm103.cuh"
 
@@ -32,7 +34,7 @@ constexpr int KSTAGES = 2;
 constexpr int VSTAGES = 2;
 constexpr int KDSTAGES = 2;
 constexpr uint32_t TMEM_COLS = 256;  // S: [0, 128), O: [128, 256)
-constexpr bool POLY_EXP = true;      // part of exp2 on the FMA pipe (see exp2_poly2)
+constexpr bool POLY_EXP = false;     // part of exp2 on the FMA pipe (see exp2_poly2); measured slower
 constexpr int CTRL_REGS = 64;
 constexpr int SOFTMAX_REGS = 192;
 static_assert(4 * 32 * CTRL_REGS + 4 * 32 * SOFTMAX_REGS == NTHREADS * 128,
@@ -135,8 +137,6 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   Smem &s = *reinterpret_cast<Smem *>(base);
-  const int KBP = kb_pad(p.Kb);
-  uint16_t *lists = reinterpret_cast<uint16_t *>(base + sizeof(Smem));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -177,12 +177,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem = s.tmem_base;
-
   if (warp < 4) {
     ptx::regs_dec<CTRL_REGS>();
     if (warp == 0) {
       // ================================================================ producer
+      const int KBP = kb_pad(p.Kb);
+      uint16_t *lists = reinterpret_cast<uint16_t *>(base + sizeof(Smem));
       const int per_qt = p.B * p.N1;
       const int ntasks = per_qt * p.Qb;
       const int npg = TILE / p.ps;
@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
     } else if (warp == 1 && lane == 0) {
       // ================================================================ MMA issuer
+      const uint32_t tmem = s.tmem_base;
       constexpr uint32_t IDESC_S = ptx::idesc_e4m3_f32(128, 128, 0);   // B = K tile, K-major
       constexpr uint32_t IDESC_PV = ptx::idesc_e4m3_f32(128, 128, 1);  // B = V tile, MN-major
       const uint32_t tS = tmem, tO = tmem + 128;
@@ -399,6 +400,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   } else {
     ptx::regs_inc<SOFTMAX_REGS>();
     // ================================================================ softmax / epilogue
+    const uint32_t tmem = s.tmem_base;
+    const int KBP = kb_pad(p.Kb);
+    const uint16_t *lists = reinterpret_cast<const uint16_t *>(base + sizeof(Smem));
     const int quad = warp & 3;  // a warp may touch TMEM lanes 32*(warp%4) .. +31
     const int r = quad * 32 + lane;
     const uint32_t tS = tmem + ((uint32_t)(quad * 32) << 16);
@@ -421,7 +425,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       const float row_scale = qd * p.scale_log2 * (p.k_per_token ? 1.f : p.k_descale[0]);
       const bool neg_scale = row_scale < 0.f;
       const int causal_lim = ti.qt * TILE + r + (ti.kv_len - ti.q_len);  // keys j <= this
-      const uint64_t rs2 = ptx::pk(row_scale, row_scale);
+      const float rs_abs = fabsf(row_scale);
+      const uint64_t rs2 = ptx::pk(rs_abs, rs_abs);
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int t = 0; t < n; ++t) {
@@ -459,22 +464,32 @@ __global__ void __launch_bounds__(NTHREADS, 2)
               x[c][j] = f2u(a);
               x[c][j + 1] = f2u(b2);
             }
-          ptx::mbar_arrive(&s.kd_empty[ds]);
+          // the slot is released with the P hand-off below, after fence.proxy.async: these are
+          // generic-proxy reads of memory the next bulk copy (async proxy) rewrites, and only a
+          // proxy fence orders the two
+        }
+        // a negative scale (never produced by amax/448 descales, but legal) is folded into the
+        // values so that one row-max path serves every row
+        if (__any_sync(0xffffffffu, neg_scale) && neg_scale) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[c][j] ^= 0x80000000u;
         }
         // number of visible keys in this tile: the rest is past the causal edge or kv_len
         int lim = ti.kv_len - tile * TILE;
         if (p.causal) lim = min(lim, causal_lim - tile * TILE + 1);
-        const bool masked = lim < TILE;
-        if (masked) {  // keep hidden keys out of the row max (or min, for a negative scale)
+        float alpha = 1.f;
+        // one specialisation per tile kind: the unmasked one carries no per-key selects
+        auto tile_body = [&](auto masked_tag) -> bool {
+          constexpr bool MASKED = decltype(masked_tag)::value;
+          if constexpr (MASKED) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (c * 32 + j >= lim) x[c][j] = f2u(neg_scale ? INFINITY : -INFINITY);
-        }
-        // row max of the unscaled values (row_scale >= 0), or row min for a negative scale
-        float mx;
-        if (!neg_scale) {
+              for (int j = 0; j < 32; ++j)
+                if (c * 32 + j >= lim) x[c][j] = f2u(-INFINITY);
+          }
           float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
@@ -483,75 +498,69 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             a2 = ptx::max3(a2, u2f(x[2][j]), u2f(x[2][j + 1]));
             a3 = ptx::max3(a3, u2f(x[3][j]), u2f(x[3][j + 1]));
           }
-          mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-        } else {
-          float a0 = INFINITY, a1 = INFINITY, a2 = INFINITY, a3 = INFINITY;
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            a0 = ptx::min3(a0, u2f(x[0][j]), u2f(x[0][j + 1]));
-            a1 = ptx::min3(a1, u2f(x[1][j]), u2f(x[1][j + 1]));
-            a2 = ptx::min3(a2, u2f(x[2][j]), u2f(x[2][j + 1]));
-            a3 = ptx::min3(a3, u2f(x[3][j]), u2f(x[3][j + 1]));
+          const float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+          // largest scaled logit of the tile (log2 units); -inf when every key is hidden
+          const float tmax = mx == -INFINITY ? -INFINITY : mx * rs_abs;
+          const float m_new = fmaxf(m, tmax);
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          alpha = ptx::ex2_approx(m - m_use);
+          const uint64_t b2 = ptx::pk(p.log2_pscale - m_use, p.log2_pscale - m_use);
+          if (t > 0) {
+            // PV(t-1) done: the P tile may be overwritten and O is stable for the rescale
+            if (!wait_bar_warp(p, s, &s.o_done, (gt - 1) & 1)) return false;
+            ptx::tc_fence_after();
           }
-          mx = fminf(fminf(a0, a1), fminf(a2, a3));
-        }
-        // largest scaled logit of the tile (log2 units); -inf when every key is hidden
-        const float tmax = (mx == INFINITY || mx == -INFINITY) ? -INFINITY : mx * row_scale;
-        const float m_new = fmaxf(m, tmax);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ptx::ex2_approx(m - m_use);
-        const uint64_t b2 = ptx::pk(p.log2_pscale - m_use, p.log2_pscale - m_use);
-        uint64_t acc0 = 0, acc1 = 0;  // packed partial sums (the 0.0f bit pattern is 0)
-        uint32_t packed[32];
+          uint64_t acc0 = 0, acc1 = 0;  // packed partial sums (the 0.0f bit pattern is 0)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk8[8];
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            float e0, e1, e2, e3;
-            ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j]), u2f(x[c][j + 1])), rs2, b2), e0, e1);
-            ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j + 2]), u2f(x[c][j + 3])), rs2, b2), e2, e3);
-            // about a third of the exponentials go to the FMA pipe, the rest to MUFU: the
-            // two units then finish a tile at about the same time
-            float p0, p1, p2, p3;
-            if (POLY_EXP && p.poly_exp && ((c * 8 + (j >> 2)) % 3) == 2) {
-              ptx::exp2_poly2(e0, e1, p0, p1);
-              ptx::exp2_poly2(e2, e3, p2, p3);
-            } else {
-              p0 = ptx::ex2_approx(e0);
-              p1 = ptx::ex2_approx(e1);
-              p2 = ptx::ex2_approx(e2);
-              p3 = ptx::ex2_approx(e3);
+            for (int j = 0; j < 32; j += 4) {
+              float e0, e1, e2, e3;
+              ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j]), u2f(x[c][j + 1])), rs2, b2), e0, e1);
+              ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j + 2]), u2f(x[c][j + 3])), rs2, b2), e2, e3);
+              if constexpr (MASKED) {  // hidden keys: exponent -inf (also when the scale is 0)
+                if (c * 32 + j + 0 >= lim) e0 = -INFINITY;
+                if (c * 32 + j + 1 >= lim) e1 = -INFINITY;
+                if (c * 32 + j + 2 >= lim) e2 = -INFINITY;
+                if (c * 32 + j + 3 >= lim) e3 = -INFINITY;
+              }
+              // about a third of the exponentials may go to the FMA pipe, the rest to MUFU
+              float p0, p1, p2, p3;
+              if (POLY_EXP && p.poly_exp && ((c * 8 + (j >> 2)) % 3) == 2) {
+                ptx::exp2_poly2(e0, e1, p0, p1);
+                ptx::exp2_poly2(e2, e3, p2, p3);
+              } else {
+                p0 = ptx::ex2_approx(e0);
+                p1 = ptx::ex2_approx(e1);
+                p2 = ptx::ex2_approx(e2);
+                p3 = ptx::ex2_approx(e3);
+              }
+              acc0 = ptx::add2(acc0, ptx::pk(p0, p1));
+              acc1 = ptx::add2(acc1, ptx::pk(p2, p3));
+              pk8[j >> 2] =
+                  (uint32_t)ptx::cvt_e4m3x2(p0, p1) | ((uint32_t)ptx::cvt_e4m3x2(p2, p3) << 16);
             }
-            if (masked) {  // hidden keys weigh exactly 0
-              if (c * 32 + j + 0 >= lim) p0 = 0.f;
-              if (c * 32 + j + 1 >= lim) p1 = 0.f;
-              if (c * 32 + j + 2 >= lim) p2 = 0.f;
-              if (c * 32 + j + 3 >= lim) p3 = 0.f;
-            }
-            acc0 = ptx::add2(acc0, ptx::pk(p0, p1));
-            acc1 = ptx::add2(acc1, ptx::pk(p2, p3));
-            packed[(c * 32 + j) >> 2] =
-                (uint32_t)ptx::cvt_e4m3x2(p0, p1) | ((uint32_t)ptx::cvt_e4m3x2(p2, p3) << 16);
+            // row r of the P tile: 8-row groups 1024 B apart, rows 128 B apart, the 16-byte
+            // chunk q of a row at chunk position q ^ (r % 8) (128-byte swizzle)
+            *reinterpret_cast<uint4 *>(prow + (((2 * c) ^ (r & 7)) << 4)) =
+                make_uint4(pk8[0], pk8[1], pk8[2], pk8[3]);
+            *reinterpret_cast<uint4 *>(prow + (((2 * c + 1) ^ (r & 7)) << 4)) =
+                make_uint4(pk8[4], pk8[5], pk8[6], pk8[7]);
           }
-        float s0, s1, s2, s3;
-        ptx::upk(acc0, s0, s1);
-        ptx::upk(acc1, s2, s3);
-        l = alpha * l + ((s0 + s1) + (s2 + s3));
-        m = m_new;
-        if (t > 0) {
-          // PV(t-1) done: the P tile may be overwritten and O is stable for the rescale
-          if (!wait_bar_warp(p, s, &s.o_done, (gt - 1) & 1)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
+          float s0, s1, s2, s3;
+          ptx::upk(acc0, s0, s1);
+          ptx::upk(acc1, s2, s3);
+          l = alpha * l + ((s0 + s1) + (s2 + s3));
+          m = m_new;
+          return true;
+        };
+        const bool body_ok = (lim < TILE) ? tile_body(std::true_type{})
+                                          : tile_body(std::false_type{});
+        if (!body_ok) {
+          ok = false;
+          break;
         }
-        // row r of the P tile: 8-row groups 1024 B apart, rows 128 B apart, the 16-byte chunk c
-        // of a row at chunk position c ^ (r % 8) (128-byte swizzle)
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4 *>(prow + ((c ^ (r & 7)) << 4)) =
-              make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
         ptx::fence_proxy_async_smem();
         if (t > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
           const uint64_t a2 = ptx::pk(alpha, alpha);
@@ -573,6 +582,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(&s.p_full);
+        if (p.k_per_token) ptx::mbar_arrive(&s.kd_empty[gt % KDSTAGES]);
       }
       if (!ok) break;
       // ---------------------------------------------------------------- epilogue
@@ -581,7 +591,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         ptx::tc_fence_after();
       }
       const float vd = p.v_per_head ? p.v_descale[g_kv] : p.v_descale[0];
-      const float osc = l > 0.f ? vd / l : 0.f;  // l carries the P-scale
+      // a row saw a visible key iff its running max is finite; l carries the P-scale
+      const bool seen = m != -INFINITY && l > 0.f;
+      const float osc = seen ? vd / l : 0.f;
       const uint64_t osc2 = ptx::pk(osc, osc);
       uint4 *orow = reinterpret_cast<uint4 *>(p.out + ((size_t)tok * p.N1 + ti.h) * HEAD_DIM);
 #pragma unroll 1
@@ -611,8 +623,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       ptx::tc_fence_before();
       ptx::mbar_arrive(&s.o_empty);
       if (row_ok && p.lse) {
-        const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f - p.ln_pscale
-                                  : -3.402823466e38f;
+        const float lse = seen ? (m + __log2f(l)) * 0.69314718055994531f - p.ln_pscale
+                               : -3.402823466e38f;
         p.lse[(size_t)ti.h * p.T + tok] = lse;
       }
       ptx::mbar_arrive(&s.task_empty[slot]);
@@ -624,7 +636,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, TMEM_COLS);
+    ptx::tmem_dealloc(s.tmem_base, TMEM_COLS);
   }
 }
 

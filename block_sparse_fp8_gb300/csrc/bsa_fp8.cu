@@ -91,6 +91,8 @@ static bsa_status_t validate_dims(const bsa_fp8_dims_t *d) {
 struct DeviceInfo {
   int state = 0;  // 0 unknown, 1 supported, 2 unsupported
   int num_sms = 0;
+  int smem_per_sm = 0;        // shared memory of one SM
+  int smem_reserved = 0;      // shared memory the system reserves per resident block
   size_t smem_attr = 0;  // dynamic shared memory the attention kernel is enabled for
 };
 
@@ -98,20 +100,26 @@ static DeviceInfo g_devices[64];
 static std::mutex g_devices_mu;
 
 // sm_103 only; caches the SM count and raises the attention kernel's shared-memory limit.
-static bsa_status_t check_device(size_t attn_smem, int *num_sms) {
+static bsa_status_t check_device(size_t attn_smem, int *num_sms, int *per_sm = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
   if (dev < 0 || dev >= 64) return BSA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_devices_mu);
   DeviceInfo &di = g_devices[dev];
   if (di.state == 0) {
-    int major = 0, minor = 0, sms = 0;
+    int major = 0, minor = 0, sms = 0, smem_sm = 0, smem_res = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_res, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+            cudaSuccess)
       return BSA_ERR_CUDA;
     di.state = (major == 10 && minor == 3) ? 1 : 2;
     di.num_sms = sms;
+    di.smem_per_sm = smem_sm;
+    di.smem_reserved = smem_res;
     if (di.state == 1) {
       // The softmax warpgroup raises its registers with setmaxnreg.inc, drawing on what the
       // CTA was launched with; that only completes if the launch allocation covers the
@@ -133,6 +141,11 @@ static bsa_status_t check_device(size_t attn_smem, int *num_sms) {
     di.smem_attr = attn_smem;
   }
   if (num_sms) *num_sms = di.num_sms;
+  if (per_sm) {
+    // the kernel is built for two resident CTAs per SM (registers, TMEM); shared memory decides
+    const size_t per_block = attn_smem + (size_t)di.smem_reserved;
+    *per_sm = (2 * per_block <= (size_t)di.smem_per_sm) ? 2 : 1;
+  }
   return BSA_OK;
 }
 
@@ -246,8 +259,8 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
       (p.k_per_token && !aligned16(k_descale)) || !aligned16(out_bf16))
     return BSA_ERR_INVALID_ARGUMENT;
   const size_t smem = attn::smem_bytes(p.Kb);
-  int num_sms = 0;
-  st = check_device(smem, &num_sms);
+  int num_sms = 0, per_sm = 1;
+  st = check_device(smem, &num_sms, &per_sm);
   if (st != BSA_OK) return st;
 
   p.q_descale = q_descale;
@@ -284,11 +297,6 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
     if (!encode_map(&tv, v_pages, 4, gd, gs, box)) return BSA_ERR_CUDA;
   }
   // persistent grid: as many CTAs as fit at once (two per SM when shared memory allows)
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn::bsa_attention_kernel,
-                                                    attn::NTHREADS, smem) != cudaSuccess ||
-      per_sm < 1)
-    return BSA_ERR_UNSUPPORTED;
   const long long grid = std::min<long long>(ntasks, (long long)per_sm * num_sms);
   attn::bsa_attention_kernel<<<(unsigned)grid, attn::NTHREADS, smem, (cudaStream_t)stream>>>(
       p, tq, tk, tv);

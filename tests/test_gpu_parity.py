@@ -281,9 +281,13 @@ def test_workload_parity(name):
     check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, f"{name} vs exact")
     check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, f"{name} vs P-emulating")
     check_lse(gl, l_ex, f"{name} lse")
+    # every task is computed by one CTA in a fixed order: repeated runs agree bit for bit
+    o_again, l_again, st = run(case, d)
+    assert st == 0 and torch.equal(out, o_again) and torch.equal(lse, l_again)
     if case.block_mask is None and case.sparse_indices is None:
         # the dense path equals an all-ones mask bit for bit
         ones = torch.ones((case.B, case.N1, case.Qb, case.Kb), dtype=torch.uint8, device="cuda")
         d2 = dict(d, block_mask=ones)
-        o2, l2, _ = run(case, d2)
-        assert torch.equal(out, o2) and torch.equal(lse, l2)
+        for _ in range(2):
+            o2, l2, st = run(case, d2)
+            assert st == 0 and torch.equal(out, o2) and torch.equal(lse, l2)
