@@ -228,6 +228,7 @@ def run_ours(args, rank, world):
     out = torch.empty((case.T, case.N1, 128), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((case.N1, case.T), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    workspace = torch.empty(max(bsa.workspace_size(dims), 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -238,7 +239,7 @@ def run_ours(args, rank, world):
                     sparse_indices=d["sparse_indices"], sparse_seq_len=d["sparse_seq_len"],
                     softmax_scale=case.softmax_scale, p_scale=case.p_scale,
                     causal=bool(case.causal), out=out, lse=lse, dev_status=status,
-                    stream=stream, k_scale_kind=case.k_scale_kind,
+                    workspace=workspace, stream=stream, k_scale_kind=case.k_scale_kind,
                     v_scale_kind=case.v_scale_kind)
 
     for _ in range(max(args.warmup, 3)):
@@ -306,8 +307,9 @@ def run_ours(args, rank, world):
                         sparse_indices=dev_in["sparse_indices"],
                         sparse_seq_len=dev_in["sparse_seq_len"],
                         softmax_scale=case.softmax_scale, p_scale=case.p_scale,
-                        causal=bool(case.causal), out=out, lse=lse, stream=stream,
-                        k_scale_kind=case.k_scale_kind, v_scale_kind=case.v_scale_kind)
+                        causal=bool(case.causal), out=out, lse=lse, workspace=workspace,
+                        stream=stream, k_scale_kind=case.k_scale_kind,
+                        v_scale_kind=case.v_scale_kind)
             host_out.copy_(out, non_blocking=True)
             host_lse.copy_(lse, non_blocking=True)
 

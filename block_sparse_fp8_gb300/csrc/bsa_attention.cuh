@@ -3,7 +3,8 @@
 // Two CTAs share each SM; each CTA walks its share of the (b, h, q-tile) tasks and owns 256
 // columns of tensor memory: S = Q K^T (fp32, 128 columns) and O (fp32, 128 columns).
 //
-//   warp 0      producer: compacts the next task's active KV tiles into a double-buffered
+//   warp 0      producer: claims the next task from a device counter (longest Q tile first),
+//               compacts its active KV tiles into a double-buffered
 //               shared list (warp ballot), publishes the task, then streams Q and, tile by
 //               tile, the K pages, the per-token K descales and the V pages through TMA
 //               (2-stage rings; masked tiles are never addressed; a missing page is read at
@@ -189,12 +190,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       int k = 0, qk = 0;
       uint32_t g = 0;
       bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const int rbase = r * (int)gridDim.x;
-        if (rbase >= ntasks) break;
-        // snake order over the task list sorted by Q tile, descending: balances causal load
-        const int o = rbase + ((r & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x);
-        if (o >= ntasks) continue;
+      for (;;) {
+        // claim the next task: tasks are numbered by Q tile, descending, so the longest causal
+        // tasks go first and a CTA that finishes early takes the next one (longest-first)
+        int o = 0;
+        if (lane == 0) o = atomicAdd(p.task_counter, 1);
+        o = __shfl_sync(0xffffffffu, o, 0);
+        if (o >= ntasks) break;
         const int qt = p.Qb - 1 - o / per_qt;
         const int rem = o % per_qt;
         const int b = rem / p.N1, h = rem % p.N1;

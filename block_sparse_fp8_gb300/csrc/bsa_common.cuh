@@ -28,6 +28,7 @@ struct Params {
   __nv_bfloat16 *out;
   float *lse;
   int *dev_status;
+  int *task_counter;  // zeroed before launch; CTAs claim task indices from it
   int B, N1, N2, G, ps, max_q_len, max_kv_len, num_pages, L, T, Qb, Kb;
   int k_per_token, v_per_head, causal;
   int poly_exp;       // 1: part of exp2 by polynomial (safe for the p_scale in use)

@@ -186,9 +186,12 @@ static bool encode_map(CUtensorMap *map, const void *base, int rank, const cuuin
 
 using namespace bsa;
 
+// one int: the task counter the persistent CTAs claim work from (padded to 256 bytes)
+static constexpr size_t WORKSPACE_BYTES = 256;
+
 extern "C" size_t bsa_fp8_prefill_workspace_size(const bsa_fp8_dims_t *dims) {
-  (void)dims;
-  return 0;  // task lists live in each CTA's shared memory
+  if (validate_dims(dims) != BSA_OK) return 0;
+  return WORKSPACE_BYTES;
 }
 
 extern "C" const char *bsa_status_string(bsa_status_t status) {
@@ -239,8 +242,6 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
                                         float p_scale, void *out_bf16, float *lse_f32,
                                         void *workspace, size_t workspace_bytes,
                                         int *dev_status, void *stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   bsa_status_t st = validate_dims(dims);
   if (st != BSA_OK) return st;
   if (block_mask && sparse_indices) return BSA_ERR_INVALID_ARGUMENT;
@@ -258,6 +259,9 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) ||
       (p.k_per_token && !aligned16(k_descale)) || !aligned16(out_bf16))
     return BSA_ERR_INVALID_ARGUMENT;
+  if (!workspace || workspace_bytes < WORKSPACE_BYTES ||
+      (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
+    return BSA_ERR_WORKSPACE;
   const size_t smem = attn::smem_bytes(p.Kb);
   int num_sms = 0, per_sm = 1;
   st = check_device(smem, &num_sms, &per_sm);
@@ -275,6 +279,7 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
   p.out = static_cast<__nv_bfloat16 *>(out_bf16);
   p.lse = lse_f32;
   p.dev_status = dev_status;
+  p.task_counter = static_cast<int *>(workspace);
   p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
   p.log2_pscale = (float)std::log2((double)p_scale);
   p.ln_pscale = (float)std::log((double)p_scale);
@@ -298,6 +303,8 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
   }
   // persistent grid: as many CTAs as fit at once (two per SM when shared memory allows)
   const long long grid = std::min<long long>(ntasks, (long long)per_sm * num_sms);
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), (cudaStream_t)stream) != cudaSuccess)
+    return BSA_ERR_CUDA;
   attn::bsa_attention_kernel<<<(unsigned)grid, attn::NTHREADS, smem, (cudaStream_t)stream>>>(
       p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;

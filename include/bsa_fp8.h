@@ -91,8 +91,10 @@ typedef struct {
   int causal;            /* 1 = right-context causal (mask_mode 3), 0 = no causal mask (mode 0) */
 } bsa_fp8_dims_t;
 
-/* Bytes of device workspace bsa_fp8_prefill needs for `dims` (0 = none; then `workspace`
- * may be NULL).  Returns 0 for invalid dims as well; bsa_fp8_prefill reports those. */
+/* Bytes of device workspace bsa_fp8_prefill needs for `dims` (currently 256: the counter
+ * the persistent kernel's CTAs claim tasks from; bsa_fp8_prefill zeroes it on `stream`
+ * before each launch, so two calls in flight at once must not share one workspace).
+ * Returns 0 for invalid dims; bsa_fp8_prefill reports those. */
 size_t bsa_fp8_prefill_workspace_size(const bsa_fp8_dims_t *dims);
 
 /* Block-sparse FP8 attention prefill over a paged KV cache.
@@ -117,8 +119,8 @@ size_t bsa_fp8_prefill_workspace_size(const bsa_fp8_dims_t *dims);
  *   p_scale         fixed P-scale; <= 0 selects the default 256; must be finite
  *   out_bf16        bf16 [T, N1, 128] (written)
  *   lse_f32         fp32 [N1, T] natural-log LSE (written), or NULL
- *   workspace       device buffer of bsa_fp8_prefill_workspace_size(dims) bytes (may be NULL
- *                   when that is 0)
+ *   workspace       device buffer of at least bsa_fp8_prefill_workspace_size(dims) bytes,
+ *                   4-byte aligned (BSA_ERR_WORKSPACE otherwise); overwritten by the call
  *   dev_status      device int, OR-ed with BSA_DEV_* bits on data errors; or NULL
  *   stream          cudaStream_t
  */

@@ -111,4 +111,16 @@ def test_compact_validation(L):
 
 
 def test_workspace_query(L):
-    assert bsa.workspace_size(_dims()) == 0
+    assert bsa.workspace_size(_dims()) == 256
+    assert bsa.workspace_size(_dims(D=64)) == 0
+
+
+def test_workspace_required(L):
+    d = _dims()
+    fake = 0x10000
+    args = [fake] * 9 + [None, None, None]
+    call = lambda ws, nbytes: L.bsa_fp8_prefill(ctypes.byref(d), *args, 0.088, 256.0, fake,
+                                                fake, ws, nbytes, None, None)
+    assert call(None, 0) == 4                 # BSA_ERR_WORKSPACE
+    assert call(0x20000, 255) == 4            # too small
+    assert call(0x20002, 256) == 4            # misaligned
