@@ -28,7 +28,7 @@ DEV_BAD_SEQLEN = 4
 DEV_TIMEOUT = 8
 
 EXPORTED = ("bsa_fp8_prefill", "bsa_fp8_prefill_workspace_size", "bsa_fp8_compact_tiles",
-            "bsa_status_string")
+            "bsa_fp8_prefill_noalloc", "bsa_status_string")
 
 
 class BsaError(RuntimeError):
@@ -60,6 +60,9 @@ def lib():
                                                                            sz, vp, vp]
         L.bsa_fp8_prefill_workspace_size.restype = sz
         L.bsa_fp8_prefill_workspace_size.argtypes = [ctypes.POINTER(Dims)]
+        L.bsa_fp8_prefill_noalloc.restype = i32
+        L.bsa_fp8_prefill_noalloc.argtypes = [ctypes.POINTER(Dims)] + [vp] * 12 + [f32, f32, vp,
+                                                                                  vp, vp, vp]
         L.bsa_fp8_compact_tiles.restype = i32
         L.bsa_fp8_compact_tiles.argtypes = [ctypes.POINTER(Dims)] + [vp] * 9
         L.bsa_status_string.restype = ctypes.c_char_p

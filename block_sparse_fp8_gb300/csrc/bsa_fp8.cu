@@ -309,3 +309,54 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
       p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
+
+// ------------------------------------------------------------------------------------------
+// bsa_fp8_prefill_noalloc: the same prefill for callers that cannot allocate device memory.
+// Its workspace is this file-scope array, 256 bytes on every device that loads the library.
+// ------------------------------------------------------------------------------------------
+
+namespace {
+
+constexpr size_t NOALLOC_SCRATCH_BYTES = 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+// Host code cannot pass g_noalloc_scratch itself to a kernel (on the host that name is only a
+// stand-in for the device symbol): look up the device address once per device, with that
+// device current, and reuse it.
+void *g_noalloc_addr[64] = {nullptr};
+std::mutex g_noalloc_mu;
+
+bsa_status_t noalloc_scratch(void **addr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return BSA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+      return BSA_ERR_CUDA;
+    g_noalloc_addr[dev] = ptr;
+  }
+  *addr = g_noalloc_addr[dev];
+  return BSA_OK;
+}
+
+}  // namespace
+
+extern "C" bsa_status_t bsa_fp8_prefill_noalloc(
+    const bsa_fp8_dims_t *dims, const void *q, const void *k_pages, const void *v_pages,
+    const float *q_descale, const float *k_descale, const float *v_descale,
+    const int *cu_seqlens_q, const int *seqused_kv, const int *block_table,
+    const uint8_t *block_mask, const int *sparse_indices, const int *sparse_seq_len,
+    float softmax_scale, float p_scale, void *out_bf16, float *lse_f32, int *dev_status,
+    void *stream) {
+  // the array is a fixed 256 bytes: a problem needing more workspace is refused, not truncated
+  if (bsa_fp8_prefill_workspace_size(dims) > NOALLOC_SCRATCH_BYTES) return BSA_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  const bsa_status_t st = noalloc_scratch(&scratch);
+  if (st != BSA_OK) return st;
+  return bsa_fp8_prefill(dims, q, k_pages, v_pages, q_descale, k_descale, v_descale,
+                         cu_seqlens_q, seqused_kv, block_table, block_mask, sparse_indices,
+                         sparse_seq_len, softmax_scale, p_scale, out_bf16, lse_f32, scratch,
+                         NOALLOC_SCRATCH_BYTES, dev_status, stream);
+}

@@ -148,6 +148,38 @@ bsa_status_t bsa_fp8_compact_tiles(const bsa_fp8_dims_t *dims, const int *cu_seq
                                    int *tile_lists, int *tile_counts, int *dev_status,
                                    void *stream);
 
+/* bsa_fp8_prefill without a caller-provided workspace.
+ *
+ * No counterpart in the pages this library implements: it exists for callers that cannot
+ * allocate device memory at the point where they run the prefill -- for example code that
+ * only receives the input and output buffers from a host application that owns every
+ * allocation (a plugin), code whose device memory comes from a fixed budget reserved at
+ * start-up, or code on a path where the implicit synchronisation of cudaMalloc/cudaFree is
+ * not acceptable.  This entry point allocates nothing: instead of `workspace` it uses a
+ * 256-byte array in the library's own device memory (every GPU that loads the library holds
+ * those 256 bytes until the process exits).
+ *
+ *   - Arguments, layouts, results and errors are exactly those of bsa_fp8_prefill, minus
+ *     `workspace` / `workspace_bytes`.  A problem whose workspace need
+ *     (bsa_fp8_prefill_workspace_size) exceeds the 256-byte array is rejected with
+ *     BSA_ERR_WORKSPACE; today every valid problem needs 256 bytes or less.
+ *   - The first call on a device (with that device current) looks up the array's device
+ *     address once; make that first call before any stream capture.  Failure of the lookup
+ *     is BSA_ERR_CUDA.
+ *   - Every call on a device shares the one array, which keeps the previous call's contents
+ *     (the call clears what must start at zero on `stream` itself).  Calls whose work
+ *     overlaps on the GPU -- on different streams without ordering between them -- race on
+ *     the array and must not be issued. */
+bsa_status_t bsa_fp8_prefill_noalloc(const bsa_fp8_dims_t *dims, const void *q,
+                                     const void *k_pages, const void *v_pages,
+                                     const float *q_descale, const float *k_descale,
+                                     const float *v_descale, const int *cu_seqlens_q,
+                                     const int *seqused_kv, const int *block_table,
+                                     const uint8_t *block_mask, const int *sparse_indices,
+                                     const int *sparse_seq_len, float softmax_scale,
+                                     float p_scale, void *out_bf16, float *lse_f32,
+                                     int *dev_status, void *stream);
+
 /* Static text for a status code. */
 const char *bsa_status_string(bsa_status_t status);
 
