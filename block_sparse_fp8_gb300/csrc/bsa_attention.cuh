@@ -1,22 +1,25 @@
 // Persistent, warp-specialised block-sparse FP8 attention prefill for sm_103a.
 //
-// Two CTAs share each SM; each CTA walks its share of the (b, h, q-tile) tasks and owns 256
-// columns of tensor memory: S = Q K^T (fp32, 128 columns) and O (fp32, 128 columns).
+// One CTA per SM runs two independent pipelines.  Each pipeline claims (b, h, q-tile) tasks
+// from a shared device counter (longest Q tile first) and owns 256 columns of tensor memory:
+// S = Q K^T (fp32, 128 columns) and O (fp32, 128 columns).  Per pipeline:
 //
-//   warp 0      producer: claims the next task from a device counter (longest Q tile first),
-//               compacts its active KV tiles into a double-buffered
-//               shared list (warp ballot), publishes the task, then streams Q and, tile by
-//               tile, the K pages, the per-token K descales and the V pages through TMA
-//               (2-stage rings; masked tiles are never addressed; a missing page is read at
-//               an out-of-range coordinate, which fills zeros).
-//   warp 1      MMA issuer (one thread): tcgen05.mma kind::f8f6f4, S(t+1) = Q K(t+1)^T as
-//               soon as the softmax has read S(t), then O (+)= P(t) V(t).
-//   warps 4-7   softmax / epilogue, one thread per query row, straight out of TMEM: scale,
-//               running max, P = 2^(x - m) at the fixed P-scale (exact zeros past the causal
-//               edge and kv_len) rounded to e4m3 into a 128B-swizzled shared tile (the A
-//               operand of the PV MMA), O rescaled in TMEM when the row max moves, and
-//               finally O * v_descale / l -> bf16, LSE -> fp32.
-//   warps 2-3   idle; the warpgroup's registers are handed to the softmax warps.
+//   producer warp   compacts the task's active KV tiles into a shared list (warp ballot),
+//                   publishes the task, then streams Q and, tile by tile, the K pages, the
+//                   per-token K descales and the V pages through TMA (2-stage rings; masked
+//                   tiles are never addressed; a missing page is read at an out-of-range
+//                   coordinate, which fills zeros).
+//   MMA warp        one thread issues tcgen05.mma kind::f8f6f4: S(t+1) = Q K(t+1)^T as soon as
+//                   the softmax has read S(t), then O (+)= P(t) V(t).
+//   2 softmax       one warpgroup per half of a tile's 128 KV columns; a thread owns one query
+//   warpgroups      row of its half: scale, the row max (the two halves exchange theirs through
+//                   shared memory), P = 2^(x - m) at the fixed P-scale (exact zeros past the
+//                   causal edge and kv_len) rounded to e4m3 into a 128B-swizzled shared tile
+//                   (the A operand of the PV MMA), O rescaled in TMEM when the row max moves,
+//                   and the epilogue O * v_descale / l -> bf16, LSE -> fp32.
+//
+// Warps 0-3 are the producers and MMA issuers of the two pipelines; warps 4-19 are the four
+// softmax warpgroups, which setmaxnreg gives most of the register file.
 //
 // Method: hpc-ops Block-Sparse FP8 Attention (活跃 tile 列表; 固定 P-scale 量化技巧) and the
 // formula of Quant Block Sparse Attention (算子介绍).
@@ -30,27 +33,33 @@
 namespace bsa {
 namespace attn {
 
-constexpr int NTHREADS = 256;
+constexpr int NPIPE = 2;
+constexpr int NTHREADS = 640;        // 4 control warps + 2 pipelines x 2 softmax warpgroups
 constexpr int KSTAGES = 2;
 constexpr int VSTAGES = 2;
 constexpr int KDSTAGES = 2;
-constexpr uint32_t TMEM_COLS = 256;  // S: [0, 128), O: [128, 256)
+constexpr uint32_t TMEM_COLS = 512;  // per pipeline: S [0, 128), O [128, 256)
 constexpr bool POLY_EXP = false;     // part of exp2 on the FMA pipe (see exp2_poly2); measured slower
-constexpr int CTRL_REGS = 64;
-constexpr int SOFTMAX_REGS = 192;
-static_assert(4 * 32 * CTRL_REGS + 4 * 32 * SOFTMAX_REGS == NTHREADS * 128,
-              "register split must add up to the launch allocation (2 CTAs per SM)");
+constexpr int CTRL_REGS = 56;
+constexpr int SOFTMAX_REGS = 104;
+// registers the split needs from the launch allocation (640 threads x 96 = 61440)
+constexpr int SPLIT_REGS = 4 * 32 * CTRL_REGS + 16 * 32 * SOFTMAX_REGS;
+static_assert(SPLIT_REGS <= NTHREADS * 96, "register split must fit 640 threads x 96 registers");
 
+// The list is ascending and every row of a Q tile sees all keys below its first row's limit,
+// so only the last two active tiles of a task can be partly hidden (causal edge, kv_len):
+// the softmax needs just their indices, carried here.
 struct TaskInfo {
-  int b, h, qt, n, q0, q_len, kv_len, pad;
+  int b, h, qt, n, q0, q_len, kv_len, tail0, tail1, pad;
 };
 
-struct __align__(1024) Smem {
+struct __align__(1024) Pipe {
   uint8_t q[TILE * HEAD_DIM];
   uint8_t k[KSTAGES][TILE * HEAD_DIM];
   uint8_t v[VSTAGES][TILE * HEAD_DIM];
   uint8_t p[TILE * HEAD_DIM];
   float kd[KDSTAGES][TILE];
+  float xbuf[2][2][TILE];  // [exchange parity][column half][row]: row max / row sum exchange
   TaskInfo info[2];
   uint32_t bitmap[KB_MAX / 32];
   uint64_t task_full[2], task_empty[2];
@@ -59,20 +68,27 @@ struct __align__(1024) Smem {
   uint64_t v_full[VSTAGES], v_empty[VSTAGES];
   uint64_t kd_full[KDSTAGES], kd_empty[KDSTAGES];
   uint64_t s_full, s_empty, p_full, o_done, o_empty, drain;
-  uint32_t tmem_base;
+  uint64_t xchg[4];  // one per 32-row quarter: the two column halves of those rows meet here
   int abort_flag;
-  // two task lists of kb_pad(Kb) uint16 follow the struct
+};
+
+struct __align__(1024) Smem {
+  Pipe pipe[NPIPE];
+  uint32_t tmem_base;
+  // one task list of kb_pad(Kb) uint16 per pipeline follows the struct
 };
 
 __host__ __device__ constexpr int kb_pad(int Kb) { return (Kb + 7) & ~7; }
 
 inline size_t smem_bytes(int Kb) {
-  return sizeof(Smem) + 2 * (size_t)kb_pad(Kb) * sizeof(uint16_t) + 1024;
+  return sizeof(Smem) + NPIPE * (size_t)kb_pad(Kb) * sizeof(uint16_t) + 1024;
 }
+static_assert(sizeof(Smem) + NPIPE * kb_pad(KB_MAX) * sizeof(uint16_t) + 1024 <= 227 * 1024,
+              "the longest task lists must fit one CTA's shared memory");
 
-// Bounded mbarrier wait.  On timeout: report, raise the CTA's abort flag and return false.
-// Returns false without waiting once another role has aborted.
-__device__ __forceinline__ bool wait_bar(const Params &p, Smem &s, uint64_t *bar,
+// Bounded mbarrier wait.  On timeout: report, raise the pipeline's abort flag and return false.
+// Returns false without waiting once another role of the pipeline has aborted.
+__device__ __forceinline__ bool wait_bar(const Params &p, Pipe &s, uint64_t *bar,
                                          uint32_t parity) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -89,8 +105,8 @@ __device__ __forceinline__ bool wait_bar(const Params &p, Smem &s, uint64_t *bar
   }
 }
 
-// Warp-uniform version for code followed by warp-collective tcgen05.ld/st.
-__device__ __forceinline__ bool wait_bar_warp(const Params &p, Smem &s, uint64_t *bar,
+// Warp-uniform version for code followed by warp-collective instructions.
+__device__ __forceinline__ bool wait_bar_warp(const Params &p, Pipe &s, uint64_t *bar,
                                               uint32_t parity) {
   return __all_sync(0xffffffffu, wait_bar(p, s, bar, parity));
 }
@@ -129,7 +145,507 @@ __device__ __forceinline__ int tile_pages(const Params &p, int b, int tile, int 
   return nvalid;
 }
 
-__global__ void __launch_bounds__(NTHREADS, 2)
+// ===================================================================================== producer
+__device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t *list,
+                                             const CUtensorMap *tmap_q,
+                                             const CUtensorMap *tmap_k,
+                                             const CUtensorMap *tmap_v) {
+  const int lane = threadIdx.x & 31;
+  const int per_qt = p.B * p.N1;
+  const int ntasks = per_qt * p.Qb;
+  const int npg = TILE / p.ps;
+  int k = 0, qk = 0;
+  uint32_t g = 0;
+  bool ok = true;
+  for (;;) {
+    // claim the next task: tasks are numbered by Q tile, descending, so the longest causal
+    // tasks go first and a pipeline that finishes early takes the next one (longest-first)
+    int o = 0;
+    if (lane == 0) o = atomicAdd(p.task_counter, 1);
+    o = __shfl_sync(0xffffffffu, o, 0);
+    if (o >= ntasks) break;
+    const int qt = p.Qb - 1 - o / per_qt;
+    const int rem = o % per_qt;
+    const int b = rem / p.N1, h = rem % p.N1;
+    const TaskGeo geo = task_geometry(p, b, qt);
+    if (!geo.valid) continue;
+    const int slot = k & 1;
+    if (k >= 2 &&
+        !__all_sync(0xffffffffu, wait_bar(p, s, &s.task_empty[slot], ((k >> 1) - 1) & 1))) {
+      ok = false;
+      break;
+    }
+    // only this warp reads the list, and it has issued every load of the previous task
+    __syncwarp();
+    const int n = compact_task(p, b, h, qt, geo.kend, list, s.bitmap);
+    if (lane == 0) {
+      TaskInfo ti;
+      ti.b = b;
+      ti.h = h;
+      ti.qt = qt;
+      ti.n = n;
+      ti.q0 = geo.q0;
+      ti.q_len = geo.q_len;
+      ti.kv_len = geo.kv_len;
+      ti.tail0 = n >= 2 ? list[n - 2] : 0;
+      ti.tail1 = n >= 1 ? list[n - 1] : 0;
+      ti.pad = 0;
+      s.info[slot] = ti;
+      ptx::mbar_arrive(&s.task_full[slot]);
+    }
+    ++k;
+    if (lane == 0 && n > 0) {
+      const int g_kv = h / p.G;
+      if (qk >= 1 && !wait_bar(p, s, &s.q_empty, (qk - 1) & 1)) ok = false;
+      if (ok) {
+        ptx::mbar_arrive_expect_tx(&s.q_full, TILE * HEAD_DIM);
+        ptx::tma_load_3d(s.q, tmap_q, &s.q_full, 0, h, geo.q0 + qt * TILE);
+      }
+      ++qk;
+      int prev[4] = {0, 0, 0, 0};
+      for (int t = 0; ok && t <= n; ++t) {
+        int pgs[4] = {0, 0, 0, 0};
+        if (t < n) {
+          const int tile = list[t];
+          const int nvalid = tile_pages(p, b, tile, geo.kv_len, pgs);
+          const uint32_t gk = g + t;
+          const int ks = gk % KSTAGES;
+          if (gk >= KSTAGES && !wait_bar(p, s, &s.k_empty[ks], ((gk / KSTAGES) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&s.k_full[ks], TILE * HEAD_DIM);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < npg)
+              ptx::tma_load_4d(s.k[ks] + i * p.ps * HEAD_DIM, tmap_k, &s.k_full[ks], 0, 0, g_kv,
+                               pgs[i]);
+          if (p.k_per_token) {
+            const int ds = gk % KDSTAGES;
+            if (gk >= KDSTAGES && !wait_bar(p, s, &s.kd_empty[ds], ((gk / KDSTAGES) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&s.kd_full[ds], (uint32_t)(nvalid * p.ps * 4));
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (i < npg && pgs[i] < p.num_pages)
+                ptx::bulk_load(&s.kd[ds][i * p.ps],
+                               p.k_descale + ((size_t)pgs[i] * p.N2 + g_kv) * p.ps,
+                               (uint32_t)(p.ps * 4), &s.kd_full[ds]);
+          }
+        }
+        if (t >= 1) {
+          // V of the previous tile: K runs one tile ahead of V, in the order the MMAs consume
+          // them (S(t) is issued before PV(t-1))
+          const uint32_t gv = g + t - 1;
+          const int vs = gv % VSTAGES;
+          if (gv >= VSTAGES && !wait_bar(p, s, &s.v_empty[vs], ((gv / VSTAGES) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&s.v_full[vs], TILE * HEAD_DIM);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < npg)
+              ptx::tma_load_4d(s.v[vs] + i * p.ps * HEAD_DIM, tmap_v, &s.v_full[vs], 0, 0, g_kv,
+                               prev[i]);
+        }
+        if (t < n) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) prev[i] = pgs[i];
+        }
+      }
+      g += n;
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    g = __shfl_sync(0xffffffffu, g, 0);
+    qk = __shfl_sync(0xffffffffu, qk, 0);
+    if (!ok) break;
+  }
+  // end-of-work marker
+  if (ok) {
+    const int slot = k & 1;
+    if (k < 2 ||
+        __all_sync(0xffffffffu, wait_bar(p, s, &s.task_empty[slot], ((k >> 1) - 1) & 1))) {
+      if (lane == 0) {
+        s.info[slot].n = -1;
+        ptx::mbar_arrive(&s.task_full[slot]);
+      }
+    }
+  }
+  if (lane == 0 && *(volatile int *)&s.abort_flag) {
+    // let the copies still in flight land before shared memory goes away
+    if (qk >= 1) drain_bar(&s.q_full, (qk - 1) & 1);
+    for (uint32_t x = g >= KSTAGES ? g - KSTAGES : 0; x < g; ++x) {
+      drain_bar(&s.k_full[x % KSTAGES], (x / KSTAGES) & 1);
+      drain_bar(&s.v_full[x % VSTAGES], (x / VSTAGES) & 1);
+      if (p.k_per_token) drain_bar(&s.kd_full[x % KDSTAGES], (x / KDSTAGES) & 1);
+    }
+  }
+}
+
+// ===================================================================================== MMA
+__device__ __forceinline__ void run_mma(const Params &p, Pipe &s, uint32_t tmem) {
+  constexpr uint32_t IDESC_S = ptx::idesc_e4m3_f32(128, 128, 0);   // B = K tile, K-major
+  constexpr uint32_t IDESC_PV = ptx::idesc_e4m3_f32(128, 128, 1);  // B = V tile, MN-major
+  const uint32_t tS = tmem, tO = tmem + 128;
+  const uint32_t q_addr = ptx::smem_u32(s.q);
+  const uint32_t p_addr = ptx::smem_u32(s.p);
+  int k = 0, qk = 0;
+  uint32_t g = 0;
+  bool ok = true;
+  auto issue_s = [&](uint32_t gs) -> bool {
+    const int ks = gs % KSTAGES;
+    if (!wait_bar(p, s, &s.k_full[ks], (gs / KSTAGES) & 1)) return false;
+    if (gs >= 1 && !wait_bar(p, s, &s.s_empty, (gs - 1) & 1)) return false;
+    ptx::tc_fence_after();
+    const uint32_t k_addr = ptx::smem_u32(s.k[ks]);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      ptx::mma_f8_ss(tS, ptx::sdesc_sw128(q_addr + 32 * kk, 16, 1024),
+                     ptx::sdesc_sw128(k_addr + 32 * kk, 16, 1024), IDESC_S, kk > 0);
+    ptx::mma_commit(&s.k_empty[ks]);
+    ptx::mma_commit(&s.s_full);
+    return true;
+  };
+  for (; ok; ++k) {
+    const int slot = k & 1;
+    if (!wait_bar(p, s, &s.task_full[slot], (k >> 1) & 1)) {
+      ok = false;
+      break;
+    }
+    const int n = s.info[slot].n;
+    if (n < 0) break;
+    if (n > 0) {
+      if (!wait_bar(p, s, &s.q_full, qk & 1)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      if (!issue_s(g)) {
+        ok = false;
+        break;
+      }
+      for (int t = 0; t < n; ++t) {
+        const uint32_t gt = g + t;
+        if (t + 1 < n) {
+          if (!issue_s(gt + 1)) {
+            ok = false;
+            break;
+          }
+        } else {
+          ptx::mma_commit(&s.q_empty);  // the task's last S has been issued
+        }
+        const int vs = gt % VSTAGES;
+        if (!wait_bar(p, s, &s.p_full, gt & 1) ||
+            !wait_bar(p, s, &s.v_full[vs], (gt / VSTAGES) & 1)) {
+          ok = false;
+          break;
+        }
+        // the previous task's epilogue must have read O before this task's first PV
+        if (t == 0 && k >= 1 && !wait_bar(p, s, &s.o_empty, (k - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t v_addr = ptx::smem_u32(s.v[vs]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_f8_ss(tO, ptx::sdesc_sw128(p_addr + 32 * kk, 16, 1024),
+                         ptx::sdesc_sw128(v_addr + 4096 * kk, 8192, 1024), IDESC_PV,
+                         (t > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(&s.v_empty[vs]);
+        ptx::mma_commit(&s.o_done);
+      }
+      if (!ok) break;
+      g += n;
+      ++qk;
+    } else if (k >= 1 && !wait_bar(p, s, &s.o_empty, (k - 1) & 1)) {
+      ok = false;  // an empty task still takes its o_empty phase, keeping phases in order
+      break;
+    }
+    ptx::mbar_arrive(&s.task_empty[slot]);
+  }
+  ptx::mma_commit(&s.drain);  // arrives once every MMA issued so far has finished
+  drain_bar(&s.drain, 0);
+}
+
+// ===================================================================================== softmax
+// Publishes `v` for row r, meets the other column half of the same 32 rows on xchg[quad] and
+// returns its value.  The two halves alternate between two buffers; neither can run two
+// exchanges ahead of the other, since each exchange needs both halves' arrivals.
+__device__ __forceinline__ bool exchange(const Params &p, Pipe &s, int quad, int half, int r,
+                                         uint32_t &xc, float v, float &other) {
+  s.xbuf[xc & 1][half][r] = v;
+  ptx::mbar_arrive(&s.xchg[quad]);
+  if (!wait_bar_warp(p, s, &s.xchg[quad], xc & 1)) return false;
+  other = s.xbuf[xc & 1][half ^ 1][r];
+  ++xc;
+  return true;
+}
+
+// Thread (half, r) owns columns [64*half, 64*half + 64) of row r of every tile.
+__device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t tmem, int half) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3;  // a warp may touch TMEM lanes 32*(warp%4) .. +31
+  const int r = quad * 32 + lane;
+  const int col0 = half * 64;
+  const uint32_t tS = tmem + ((uint32_t)(quad * 32) << 16) + col0;
+  const uint32_t tO = tS + 128;
+  uint8_t *prow = s.p + (r >> 3) * 1024 + (r & 7) * 128;
+  uint32_t xc = 0;
+  int k = 0;
+  uint32_t g = 0;
+  for (;; ++k) {
+    const int slot = k & 1;
+    if (!wait_bar_warp(p, s, &s.task_full[slot], (k >> 1) & 1)) break;
+    // the task's record stays put until this task's task_empty arrival: fields are read from
+    // shared memory where they are used rather than held in registers across the tile loop
+    const TaskInfo &ti = s.info[slot];
+    const int n = ti.n;
+    if (n < 0) break;
+    float row_scale;
+    int causal_lim;  // keys j <= causal_lim are visible to row r
+    {
+      const int qt = ti.qt, h = ti.h, q_len = ti.q_len;
+      const int tok = ti.q0 + qt * TILE + r;
+      const float qd =
+          r < min(TILE, q_len - qt * TILE) ? p.q_descale[(size_t)tok * p.N1 + h] : 0.f;
+      row_scale = qd * p.scale_log2 * (p.k_per_token ? 1.f : p.k_descale[0]);
+      causal_lim = qt * TILE + r + (ti.kv_len - q_len);
+    }
+    const bool neg_scale = row_scale < 0.f;
+    const float rs_abs = fabsf(row_scale);
+    const uint64_t rs2 = ptx::pk(rs_abs, rs_abs);
+    float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      const uint32_t gt = g + t;
+      if (!wait_bar_warp(p, s, &s.s_full, gt & 1)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      uint32_t x[2][32];
+      ptx::tmem_ld32(tS, x[0]);
+      ptx::tmem_ld32(tS + 32, x[1]);
+      ptx::tmem_ld_wait(x[0]);
+      ptx::reg_fence(x[1]);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&s.s_empty);
+
+      if (p.k_per_token) {
+        const int ds = gt % KDSTAGES;
+        if (!wait_bar_warp(p, s, &s.kd_full[ds], (gt / KDSTAGES) & 1)) {
+          ok = false;
+          break;
+        }
+        const ulonglong2 *kd4 = reinterpret_cast<const ulonglong2 *>(&s.kd[ds][col0]);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const ulonglong2 kv = kd4[(c * 32 + j) >> 2];  // 4 descales per 16-byte load
+            float a0, a1, a2, a3;
+            ptx::upk(ptx::mul2(ptx::pk(u2f(x[c][j]), u2f(x[c][j + 1])), kv.x), a0, a1);
+            ptx::upk(ptx::mul2(ptx::pk(u2f(x[c][j + 2]), u2f(x[c][j + 3])), kv.y), a2, a3);
+            x[c][j] = f2u(a0);
+            x[c][j + 1] = f2u(a1);
+            x[c][j + 2] = f2u(a2);
+            x[c][j + 3] = f2u(a3);
+          }
+        // the slot is released with the P hand-off below, after fence.proxy.async: these are
+        // generic-proxy reads of memory the next bulk copy (async proxy) rewrites, and only a
+        // proxy fence orders the two
+      }
+      // a negative scale (never produced by amax/448 descales, but legal) is folded into the
+      // values so that one row-max path serves every row
+      if (__any_sync(0xffffffffu, neg_scale) && neg_scale) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[c][j] ^= 0x80000000u;
+      }
+      // visible keys of this half of the tile (the rest lies past the causal edge or
+      // kv_len); only the task's last two tiles can have any hidden key
+      int lim = 64;
+      if (t + 2 >= n) {
+        const int tile = (t + 2 == n) ? ti.tail0 : ti.tail1;
+        lim = ti.kv_len - tile * TILE;
+        if (p.causal) lim = min(lim, causal_lim - tile * TILE + 1);
+        lim -= col0;
+      }
+      float alpha = 1.f;
+      uint32_t packed[16];  // this half of the row of P as e4m3, 4 keys per word
+      // one specialisation per tile kind: the unmasked one carries no per-key selects
+      auto tile_body = [&](auto masked_tag) -> bool {
+        constexpr bool MASKED = decltype(masked_tag)::value;
+        if constexpr (MASKED) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c * 32 + j >= lim) x[c][j] = f2u(-INFINITY);
+        }
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          a0 = ptx::max3(a0, u2f(x[0][j]), u2f(x[0][j + 1]));
+          a1 = ptx::max3(a1, u2f(x[0][j + 2]), u2f(x[0][j + 3]));
+          a2 = ptx::max3(a2, u2f(x[1][j]), u2f(x[1][j + 1]));
+          a3 = ptx::max3(a3, u2f(x[1][j + 2]), u2f(x[1][j + 3]));
+        }
+        float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+        float mx_other = -INFINITY;
+        if (!exchange(p, s, quad, half, r, xc, mx, mx_other)) return false;
+        mx = fmaxf(mx, mx_other);  // the same value in both halves
+        // largest scaled logit of the tile (log2 units); -inf when every key is hidden
+        const float tmax = mx == -INFINITY ? -INFINITY : mx * rs_abs;
+        const float m_new = fmaxf(m, tmax);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        alpha = ptx::ex2_approx(m - m_use);
+        const uint64_t b2 = ptx::pk(p.log2_pscale - m_use, p.log2_pscale - m_use);
+        uint64_t acc0 = 0, acc1 = 0;  // packed partial sums (the 0.0f bit pattern is 0)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float e0, e1, e2, e3;
+            ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j]), u2f(x[c][j + 1])), rs2, b2), e0, e1);
+            ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j + 2]), u2f(x[c][j + 3])), rs2, b2), e2, e3);
+            if constexpr (MASKED) {  // hidden keys: exponent -inf (also when the scale is 0)
+              if (c * 32 + j + 0 >= lim) e0 = -INFINITY;
+              if (c * 32 + j + 1 >= lim) e1 = -INFINITY;
+              if (c * 32 + j + 2 >= lim) e2 = -INFINITY;
+              if (c * 32 + j + 3 >= lim) e3 = -INFINITY;
+            }
+            float p0, p1, p2, p3;
+            if (POLY_EXP && p.poly_exp && ((c * 8 + (j >> 2)) % 3) == 2) {
+              ptx::exp2_poly2(e0, e1, p0, p1);
+              ptx::exp2_poly2(e2, e3, p2, p3);
+            } else {
+              p0 = ptx::ex2_approx(e0);
+              p1 = ptx::ex2_approx(e1);
+              p2 = ptx::ex2_approx(e2);
+              p3 = ptx::ex2_approx(e3);
+            }
+            acc0 = ptx::add2(acc0, ptx::pk(p0, p1));
+            acc1 = ptx::add2(acc1, ptx::pk(p2, p3));
+            packed[(c * 32 + j) >> 2] =
+                (uint32_t)ptx::cvt_e4m3x2(p0, p1) | ((uint32_t)ptx::cvt_e4m3x2(p2, p3) << 16);
+          }
+        float s0, s1, s2, s3;
+        ptx::upk(acc0, s0, s1);
+        ptx::upk(acc1, s2, s3);
+        l = alpha * l + ((s0 + s1) + (s2 + s3));
+        m = m_new;
+        return true;
+      };
+      const bool body_ok =
+          (lim < 64) ? tile_body(std::true_type{}) : tile_body(std::false_type{});
+      if (!body_ok) {
+        ok = false;
+        break;
+      }
+      if (t > 0) {
+        // PV(t-1) done: the P tile may be overwritten and O is stable for the rescale
+        if (!wait_bar_warp(p, s, &s.o_done, (gt - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+      }
+      // row r of the P tile: 8-row groups 1024 B apart, rows 128 B apart, the 16-byte chunk q
+      // of a row at chunk position q ^ (r % 8) (128-byte swizzle); this half owns chunks
+      // 4*half .. 4*half + 3
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(prow + (((4 * half + q) ^ (r & 7)) << 4)) =
+            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+      ptx::fence_proxy_async_smem();
+      if (t > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
+        // O *= alpha on this half's 64 columns of the warp's rows
+        const uint64_t a2 = ptx::pk(alpha, alpha);
+        uint32_t o[2][32];
+        ptx::tmem_ld32(tO, o[0]);
+        ptx::tmem_ld32(tO + 32, o[1]);
+        ptx::tmem_ld_wait(o[0]);
+        ptx::reg_fence(o[1]);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float a, b3;
+            ptx::upk(ptx::mul2(ptx::pk(u2f(o[c][j]), u2f(o[c][j + 1])), a2), a, b3);
+            o[c][j] = f2u(a);
+            o[c][j + 1] = f2u(b3);
+          }
+          ptx::tmem_st32(tO + c * 32, o[c]);
+        }
+        ptx::tmem_st_wait();
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&s.p_full);
+      if (p.k_per_token) ptx::mbar_arrive(&s.kd_empty[gt % KDSTAGES]);
+    }
+    if (!ok) break;
+    // ------------------------------------------------------------------------- epilogue
+    const int h = ti.h, qt = ti.qt;
+    const bool row_ok = r < min(TILE, ti.q_len - qt * TILE);
+    const int tok = ti.q0 + qt * TILE + r;
+    const int g_kv = h / p.G;
+    float l_other = 0.f;
+    if (!exchange(p, s, quad, half, r, xc, l, l_other)) break;
+    const float l_row = l + l_other;  // both halves kept the same running max
+    if (n > 0) {
+      if (!wait_bar_warp(p, s, &s.o_done, (g + n - 1) & 1)) break;
+      ptx::tc_fence_after();
+    }
+    // a row saw a visible key iff its running max is finite; l_row carries the P-scale
+    const bool seen = m != -INFINITY && l_row > 0.f;
+    const float vd = p.v_per_head ? p.v_descale[g_kv] : p.v_descale[0];
+    const float osc = seen ? vd / l_row : 0.f;
+    const uint64_t osc2 = ptx::pk(osc, osc);
+    uint4 *orow =
+        reinterpret_cast<uint4 *>(p.out + ((size_t)tok * p.N1 + h) * HEAD_DIM + col0);
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+      uint32_t o[32];
+      if (n > 0) {
+        ptx::tmem_ld32(tO + c * 32, o);
+        ptx::tmem_ld_wait(o);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = 0u;
+      }
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float a, b3;
+        ptx::upk(ptx::mul2(ptx::pk(u2f(o[2 * j]), u2f(o[2 * j + 1])), osc2), a, b3);
+        __nv_bfloat162 v2 = __floats2bfloat162_rn(a, b3);
+        w[j] = *reinterpret_cast<uint32_t *>(&v2);
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          orow[c * 4 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      }
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(&s.o_empty);
+    if (half == 0 && row_ok && p.lse) {
+      const float lse = seen ? (m + __log2f(l_row)) * 0.69314718055994531f - p.ln_pscale
+                             : -3.402823466e38f;
+      p.lse[(size_t)h * p.T + tok] = lse;
+    }
+    ptx::mbar_arrive(&s.task_empty[slot]);
+    g += n;
+  }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
     bsa_attention_kernel(const __grid_constant__ Params p,
                          const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ CUtensorMap tmap_k,
@@ -137,13 +653,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  Smem &s = *reinterpret_cast<Smem *>(base);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Smem &sm = *reinterpret_cast<Smem *>(base);
+  const int warp = threadIdx.x >> 5;
 
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < NPIPE) {
+    Pipe &s = sm.pipe[threadIdx.x];
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&s.task_full[i], 1);
-      ptx::mbar_init(&s.task_empty[i], 128 + 1);
+      ptx::mbar_init(&s.task_empty[i], 256 + 1);  // both softmax warpgroups + the MMA thread
     }
     ptx::mbar_init(&s.q_full, 1);
     ptx::mbar_init(&s.q_empty, 1);
@@ -157,488 +674,53 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
     for (int i = 0; i < KDSTAGES; ++i) {
       ptx::mbar_init(&s.kd_full[i], 1);
-      ptx::mbar_init(&s.kd_empty[i], 128);
+      ptx::mbar_init(&s.kd_empty[i], 256);
     }
     ptx::mbar_init(&s.s_full, 1);
-    ptx::mbar_init(&s.s_empty, 128);
-    ptx::mbar_init(&s.p_full, 128);
+    ptx::mbar_init(&s.s_empty, 256);
+    ptx::mbar_init(&s.p_full, 256);
     ptx::mbar_init(&s.o_done, 1);
-    ptx::mbar_init(&s.o_empty, 128);
+    ptx::mbar_init(&s.o_empty, 256);
     ptx::mbar_init(&s.drain, 1);
+    for (int i = 0; i < 4; ++i) ptx::mbar_init(&s.xchg[i], 64);  // two warps, one per half
     s.abort_flag = 0;
     ptx::fence_mbarrier_init();
-    ptx::prefetch_tmap(&tmap_q);
-    ptx::prefetch_tmap(&tmap_k);
-    ptx::prefetch_tmap(&tmap_v);
+    if (threadIdx.x == 0) {
+      ptx::prefetch_tmap(&tmap_q);
+      ptx::prefetch_tmap(&tmap_k);
+      ptx::prefetch_tmap(&tmap_v);
+    }
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&s.tmem_base, TMEM_COLS);
+    ptx::tmem_alloc(&sm.tmem_base, TMEM_COLS);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+
   if (warp < 4) {
     ptx::regs_dec<CTRL_REGS>();
-    if (warp == 0) {
-      // ================================================================ producer
-      const int KBP = kb_pad(p.Kb);
-      uint16_t *lists = reinterpret_cast<uint16_t *>(base + sizeof(Smem));
-      const int per_qt = p.B * p.N1;
-      const int ntasks = per_qt * p.Qb;
-      const int npg = TILE / p.ps;
-      int k = 0, qk = 0;
-      uint32_t g = 0;
-      bool ok = true;
-      for (;;) {
-        // claim the next task: tasks are numbered by Q tile, descending, so the longest causal
-        // tasks go first and a CTA that finishes early takes the next one (longest-first)
-        int o = 0;
-        if (lane == 0) o = atomicAdd(p.task_counter, 1);
-        o = __shfl_sync(0xffffffffu, o, 0);
-        if (o >= ntasks) break;
-        const int qt = p.Qb - 1 - o / per_qt;
-        const int rem = o % per_qt;
-        const int b = rem / p.N1, h = rem % p.N1;
-        const TaskGeo geo = task_geometry(p, b, qt);
-        if (!geo.valid) continue;
-        const int slot = k & 1;
-        if (k >= 2 && !__all_sync(0xffffffffu,
-                                  wait_bar(p, s, &s.task_empty[slot], ((k >> 1) - 1) & 1))) {
-          ok = false;
-          break;
-        }
-        uint16_t *list = lists + slot * KBP;
-        const int n = compact_task(p, b, h, qt, geo.kend, list, s.bitmap);
-        if (lane == 0) {
-          TaskInfo ti;
-          ti.b = b;
-          ti.h = h;
-          ti.qt = qt;
-          ti.n = n;
-          ti.q0 = geo.q0;
-          ti.q_len = geo.q_len;
-          ti.kv_len = geo.kv_len;
-          ti.pad = 0;
-          s.info[slot] = ti;
-          ptx::mbar_arrive(&s.task_full[slot]);
-        }
-        ++k;
-        if (lane == 0 && n > 0) {
-          const int g_kv = h / p.G;
-          if (qk >= 1 && !wait_bar(p, s, &s.q_empty, (qk - 1) & 1)) ok = false;
-          if (ok) {
-            ptx::mbar_arrive_expect_tx(&s.q_full, TILE * HEAD_DIM);
-            ptx::tma_load_3d(s.q, &tmap_q, &s.q_full, 0, h, geo.q0 + qt * TILE);
-          }
-          ++qk;
-          int prev[4] = {0, 0, 0, 0};
-          for (int t = 0; ok && t <= n; ++t) {
-            int pgs[4] = {0, 0, 0, 0};
-            if (t < n) {
-              const int tile = list[t];
-              const int nvalid = tile_pages(p, b, tile, geo.kv_len, pgs);
-              const uint32_t gk = g + t;
-              const int ks = gk % KSTAGES;
-              if (gk >= KSTAGES && !wait_bar(p, s, &s.k_empty[ks], ((gk / KSTAGES) - 1) & 1)) {
-                ok = false;
-                break;
-              }
-              ptx::mbar_arrive_expect_tx(&s.k_full[ks], TILE * HEAD_DIM);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                if (i < npg)
-                  ptx::tma_load_4d(s.k[ks] + i * p.ps * HEAD_DIM, &tmap_k, &s.k_full[ks], 0, 0,
-                                   g_kv, pgs[i]);
-              if (p.k_per_token) {
-                const int ds = gk % KDSTAGES;
-                if (gk >= KDSTAGES &&
-                    !wait_bar(p, s, &s.kd_empty[ds], ((gk / KDSTAGES) - 1) & 1)) {
-                  ok = false;
-                  break;
-                }
-                ptx::mbar_arrive_expect_tx(&s.kd_full[ds], (uint32_t)(nvalid * p.ps * 4));
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  if (i < npg && pgs[i] < p.num_pages)
-                    ptx::bulk_load(&s.kd[ds][i * p.ps],
-                                   p.k_descale + ((size_t)pgs[i] * p.N2 + g_kv) * p.ps,
-                                   (uint32_t)(p.ps * 4), &s.kd_full[ds]);
-              }
-            }
-            if (t >= 1) {
-              // V of the previous tile: K runs one tile ahead of V, in the order the MMAs
-              // consume them (S(t) is issued before PV(t-1))
-              const uint32_t gv = g + t - 1;
-              const int vs = gv % VSTAGES;
-              if (gv >= VSTAGES && !wait_bar(p, s, &s.v_empty[vs], ((gv / VSTAGES) - 1) & 1)) {
-                ok = false;
-                break;
-              }
-              ptx::mbar_arrive_expect_tx(&s.v_full[vs], TILE * HEAD_DIM);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                if (i < npg)
-                  ptx::tma_load_4d(s.v[vs] + i * p.ps * HEAD_DIM, &tmap_v, &s.v_full[vs], 0, 0,
-                                   g_kv, prev[i]);
-            }
-            if (t < n) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) prev[i] = pgs[i];
-            }
-          }
-          g += n;
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        g = __shfl_sync(0xffffffffu, g, 0);
-        qk = __shfl_sync(0xffffffffu, qk, 0);
-      }
-      // end-of-work marker
-      if (ok) {
-        const int slot = k & 1;
-        if (k < 2 || __all_sync(0xffffffffu,
-                                wait_bar(p, s, &s.task_empty[slot], ((k >> 1) - 1) & 1))) {
-          if (lane == 0) {
-            s.info[slot].n = -1;
-            ptx::mbar_arrive(&s.task_full[slot]);
-          }
-        }
-      }
-      if (lane == 0 && *(volatile int *)&s.abort_flag) {
-        // let the copies still in flight land before shared memory goes away
-        if (qk >= 1) drain_bar(&s.q_full, (qk - 1) & 1);
-        for (uint32_t x = g >= KSTAGES ? g - KSTAGES : 0; x < g; ++x) {
-          drain_bar(&s.k_full[x % KSTAGES], (x / KSTAGES) & 1);
-          drain_bar(&s.v_full[x % VSTAGES], (x / VSTAGES) & 1);
-          if (p.k_per_token) drain_bar(&s.kd_full[x % KDSTAGES], (x / KDSTAGES) & 1);
-        }
-      }
-    } else if (warp == 1 && lane == 0) {
-      // ================================================================ MMA issuer
-      const uint32_t tmem = s.tmem_base;
-      constexpr uint32_t IDESC_S = ptx::idesc_e4m3_f32(128, 128, 0);   // B = K tile, K-major
-      constexpr uint32_t IDESC_PV = ptx::idesc_e4m3_f32(128, 128, 1);  // B = V tile, MN-major
-      const uint32_t tS = tmem, tO = tmem + 128;
-      const uint32_t q_addr = ptx::smem_u32(s.q);
-      const uint32_t p_addr = ptx::smem_u32(s.p);
-      int k = 0, qk = 0;
-      uint32_t g = 0;
-      bool ok = true;
-      auto issue_s = [&](uint32_t gs) -> bool {
-        const int ks = gs % KSTAGES;
-        if (!wait_bar(p, s, &s.k_full[ks], (gs / KSTAGES) & 1)) return false;
-        if (gs >= 1 && !wait_bar(p, s, &s.s_empty, (gs - 1) & 1)) return false;
-        ptx::tc_fence_after();
-        const uint32_t k_addr = ptx::smem_u32(s.k[ks]);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_f8_ss(tS, ptx::sdesc_sw128(q_addr + 32 * kk, 16, 1024),
-                         ptx::sdesc_sw128(k_addr + 32 * kk, 16, 1024), IDESC_S, kk > 0);
-        ptx::mma_commit(&s.k_empty[ks]);
-        ptx::mma_commit(&s.s_full);
-        return true;
-      };
-      for (; ok; ++k) {
-        const int slot = k & 1;
-        if (!wait_bar(p, s, &s.task_full[slot], (k >> 1) & 1)) {
-          ok = false;
-          break;
-        }
-        const int n = s.info[slot].n;
-        if (n < 0) break;
-        if (n > 0) {
-          if (!wait_bar(p, s, &s.q_full, qk & 1)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          if (!issue_s(g)) {
-            ok = false;
-            break;
-          }
-          for (int t = 0; t < n; ++t) {
-            const uint32_t gt = g + t;
-            if (t + 1 < n) {
-              if (!issue_s(gt + 1)) {
-                ok = false;
-                break;
-              }
-            } else {
-              ptx::mma_commit(&s.q_empty);  // the task's last S has been issued
-            }
-            const int vs = gt % VSTAGES;
-            if (!wait_bar(p, s, &s.p_full, gt & 1) ||
-                !wait_bar(p, s, &s.v_full[vs], (gt / VSTAGES) & 1)) {
-              ok = false;
-              break;
-            }
-            // the previous task's epilogue must have read O before this task's first PV
-            if (t == 0 && k >= 1 && !wait_bar(p, s, &s.o_empty, (k - 1) & 1)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t v_addr = ptx::smem_u32(s.v[vs]);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              ptx::mma_f8_ss(tO, ptx::sdesc_sw128(p_addr + 32 * kk, 16, 1024),
-                             ptx::sdesc_sw128(v_addr + 4096 * kk, 8192, 1024), IDESC_PV,
-                             (t > 0 || kk > 0) ? 1u : 0u);
-            ptx::mma_commit(&s.v_empty[vs]);
-            ptx::mma_commit(&s.o_done);
-          }
-          if (!ok) break;
-          g += n;
-          ++qk;
-        } else if (k >= 1 && !wait_bar(p, s, &s.o_empty, (k - 1) & 1)) {
-          ok = false;  // an empty task still takes its o_empty phase, keeping phases in order
-          break;
-        }
-        ptx::mbar_arrive(&s.task_empty[slot]);
-      }
-      ptx::mma_commit(&s.drain);  // arrives once every MMA issued so far has finished
-      drain_bar(&s.drain, 0);
+    const int pipe = warp >> 1;
+    Pipe &s = sm.pipe[pipe];
+    if ((warp & 1) == 0) {
+      uint16_t *list = reinterpret_cast<uint16_t *>(base + sizeof(Smem)) + pipe * kb_pad(p.Kb);
+      run_producer(p, s, list, &tmap_q, &tmap_k, &tmap_v);
+    } else if ((threadIdx.x & 31) == 0) {
+      run_mma(p, s, sm.tmem_base + 256u * pipe);
     }
   } else {
     ptx::regs_inc<SOFTMAX_REGS>();
-    // ================================================================ softmax / epilogue
-    const uint32_t tmem = s.tmem_base;
-    const int KBP = kb_pad(p.Kb);
-    const uint16_t *lists = reinterpret_cast<const uint16_t *>(base + sizeof(Smem));
-    const int quad = warp & 3;  // a warp may touch TMEM lanes 32*(warp%4) .. +31
-    const int r = quad * 32 + lane;
-    const uint32_t tS = tmem + ((uint32_t)(quad * 32) << 16);
-    const uint32_t tO = tS + 128;
-    uint8_t *prow = s.p + (r >> 3) * 1024 + (r & 7) * 128;
-    int k = 0;
-    uint32_t g = 0;
-    for (;; ++k) {
-      const int slot = k & 1;
-      if (!wait_bar_warp(p, s, &s.task_full[slot], (k >> 1) & 1)) break;
-      const TaskInfo ti = s.info[slot];
-      if (ti.n < 0) break;
-      const uint16_t *list = lists + slot * KBP;
-      const int n = ti.n;
-      const int g_kv = ti.h / p.G;
-      const int rows_valid = min(TILE, ti.q_len - ti.qt * TILE);
-      const bool row_ok = r < rows_valid;
-      const int tok = ti.q0 + ti.qt * TILE + r;
-      const float qd = row_ok ? p.q_descale[(size_t)tok * p.N1 + ti.h] : 0.f;
-      const float row_scale = qd * p.scale_log2 * (p.k_per_token ? 1.f : p.k_descale[0]);
-      const bool neg_scale = row_scale < 0.f;
-      const int causal_lim = ti.qt * TILE + r + (ti.kv_len - ti.q_len);  // keys j <= this
-      const float rs_abs = fabsf(row_scale);
-      const uint64_t rs2 = ptx::pk(rs_abs, rs_abs);
-      float m = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int t = 0; t < n; ++t) {
-        const uint32_t gt = g + t;
-        const int tile = list[t];
-        if (!wait_bar_warp(p, s, &s.s_full, gt & 1)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        uint32_t x[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, x[c]);
-        ptx::tmem_ld_wait(x[0]);
-        ptx::reg_fence(x[1]);
-        ptx::reg_fence(x[2]);
-        ptx::reg_fence(x[3]);
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&s.s_empty);
-
-        if (p.k_per_token) {
-          const int ds = gt % KDSTAGES;
-          if (!wait_bar_warp(p, s, &s.kd_full[ds], (gt / KDSTAGES) & 1)) {
-            ok = false;
-            break;
-          }
-          const uint64_t *kd2 = reinterpret_cast<const uint64_t *>(s.kd[ds]);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float a, b2;
-              ptx::upk(ptx::mul2(ptx::pk(u2f(x[c][j]), u2f(x[c][j + 1])), kd2[(c * 32 + j) >> 1]),
-                       a, b2);
-              x[c][j] = f2u(a);
-              x[c][j + 1] = f2u(b2);
-            }
-          // the slot is released with the P hand-off below, after fence.proxy.async: these are
-          // generic-proxy reads of memory the next bulk copy (async proxy) rewrites, and only a
-          // proxy fence orders the two
-        }
-        // a negative scale (never produced by amax/448 descales, but legal) is folded into the
-        // values so that one row-max path serves every row
-        if (__any_sync(0xffffffffu, neg_scale) && neg_scale) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x[c][j] ^= 0x80000000u;
-        }
-        // number of visible keys in this tile: the rest is past the causal edge or kv_len
-        int lim = ti.kv_len - tile * TILE;
-        if (p.causal) lim = min(lim, causal_lim - tile * TILE + 1);
-        float alpha = 1.f;
-        // one specialisation per tile kind: the unmasked one carries no per-key selects
-        auto tile_body = [&](auto masked_tag) -> bool {
-          constexpr bool MASKED = decltype(masked_tag)::value;
-          if constexpr (MASKED) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (c * 32 + j >= lim) x[c][j] = f2u(-INFINITY);
-          }
-          float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            a0 = ptx::max3(a0, u2f(x[0][j]), u2f(x[0][j + 1]));
-            a1 = ptx::max3(a1, u2f(x[1][j]), u2f(x[1][j + 1]));
-            a2 = ptx::max3(a2, u2f(x[2][j]), u2f(x[2][j + 1]));
-            a3 = ptx::max3(a3, u2f(x[3][j]), u2f(x[3][j + 1]));
-          }
-          const float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-          // largest scaled logit of the tile (log2 units); -inf when every key is hidden
-          const float tmax = mx == -INFINITY ? -INFINITY : mx * rs_abs;
-          const float m_new = fmaxf(m, tmax);
-          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-          alpha = ptx::ex2_approx(m - m_use);
-          const uint64_t b2 = ptx::pk(p.log2_pscale - m_use, p.log2_pscale - m_use);
-          if (t > 0) {
-            // PV(t-1) done: the P tile may be overwritten and O is stable for the rescale
-            if (!wait_bar_warp(p, s, &s.o_done, (gt - 1) & 1)) return false;
-            ptx::tc_fence_after();
-          }
-          uint64_t acc0 = 0, acc1 = 0;  // packed partial sums (the 0.0f bit pattern is 0)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk8[8];
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              float e0, e1, e2, e3;
-              ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j]), u2f(x[c][j + 1])), rs2, b2), e0, e1);
-              ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j + 2]), u2f(x[c][j + 3])), rs2, b2), e2, e3);
-              if constexpr (MASKED) {  // hidden keys: exponent -inf (also when the scale is 0)
-                if (c * 32 + j + 0 >= lim) e0 = -INFINITY;
-                if (c * 32 + j + 1 >= lim) e1 = -INFINITY;
-                if (c * 32 + j + 2 >= lim) e2 = -INFINITY;
-                if (c * 32 + j + 3 >= lim) e3 = -INFINITY;
-              }
-              // about a third of the exponentials may go to the FMA pipe, the rest to MUFU
-              float p0, p1, p2, p3;
-              if (POLY_EXP && p.poly_exp && ((c * 8 + (j >> 2)) % 3) == 2) {
-                ptx::exp2_poly2(e0, e1, p0, p1);
-                ptx::exp2_poly2(e2, e3, p2, p3);
-              } else {
-                p0 = ptx::ex2_approx(e0);
-                p1 = ptx::ex2_approx(e1);
-                p2 = ptx::ex2_approx(e2);
-                p3 = ptx::ex2_approx(e3);
-              }
-              acc0 = ptx::add2(acc0, ptx::pk(p0, p1));
-              acc1 = ptx::add2(acc1, ptx::pk(p2, p3));
-              pk8[j >> 2] =
-                  (uint32_t)ptx::cvt_e4m3x2(p0, p1) | ((uint32_t)ptx::cvt_e4m3x2(p2, p3) << 16);
-            }
-            // row r of the P tile: 8-row groups 1024 B apart, rows 128 B apart, the 16-byte
-            // chunk q of a row at chunk position q ^ (r % 8) (128-byte swizzle)
-            *reinterpret_cast<uint4 *>(prow + (((2 * c) ^ (r & 7)) << 4)) =
-                make_uint4(pk8[0], pk8[1], pk8[2], pk8[3]);
-            *reinterpret_cast<uint4 *>(prow + (((2 * c + 1) ^ (r & 7)) << 4)) =
-                make_uint4(pk8[4], pk8[5], pk8[6], pk8[7]);
-          }
-          float s0, s1, s2, s3;
-          ptx::upk(acc0, s0, s1);
-          ptx::upk(acc1, s2, s3);
-          l = alpha * l + ((s0 + s1) + (s2 + s3));
-          m = m_new;
-          return true;
-        };
-        const bool body_ok = (lim < TILE) ? tile_body(std::true_type{})
-                                          : tile_body(std::false_type{});
-        if (!body_ok) {
-          ok = false;
-          break;
-        }
-        ptx::fence_proxy_async_smem();
-        if (t > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
-          const uint64_t a2 = ptx::pk(alpha, alpha);
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + c * 32, o);
-            ptx::tmem_ld_wait(o);
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float a, b3;
-              ptx::upk(ptx::mul2(ptx::pk(u2f(o[j]), u2f(o[j + 1])), a2), a, b3);
-              o[j] = f2u(a);
-              o[j + 1] = f2u(b3);
-            }
-            ptx::tmem_st32(tO + c * 32, o);
-          }
-          ptx::tmem_st_wait();
-        }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&s.p_full);
-        if (p.k_per_token) ptx::mbar_arrive(&s.kd_empty[gt % KDSTAGES]);
-      }
-      if (!ok) break;
-      // ---------------------------------------------------------------- epilogue
-      if (n > 0) {
-        if (!wait_bar_warp(p, s, &s.o_done, (g + n - 1) & 1)) break;
-        ptx::tc_fence_after();
-      }
-      const float vd = p.v_per_head ? p.v_descale[g_kv] : p.v_descale[0];
-      // a row saw a visible key iff its running max is finite; l carries the P-scale
-      const bool seen = m != -INFINITY && l > 0.f;
-      const float osc = seen ? vd / l : 0.f;
-      const uint64_t osc2 = ptx::pk(osc, osc);
-      uint4 *orow = reinterpret_cast<uint4 *>(p.out + ((size_t)tok * p.N1 + ti.h) * HEAD_DIM);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        if (n > 0) {
-          ptx::tmem_ld32(tO + c * 32, o);
-          ptx::tmem_ld_wait(o);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = 0u;
-        }
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float a, b3;
-          ptx::upk(ptx::mul2(ptx::pk(u2f(o[2 * j]), u2f(o[2 * j + 1])), osc2), a, b3);
-          __nv_bfloat162 v2 = __floats2bfloat162_rn(a, b3);
-          w[j] = *reinterpret_cast<uint32_t *>(&v2);
-        }
-        if (row_ok) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            orow[c * 4 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-        }
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&s.o_empty);
-      if (row_ok && p.lse) {
-        const float lse = seen ? (m + __log2f(l)) * 0.69314718055994531f - p.ln_pscale
-                               : -3.402823466e38f;
-        p.lse[(size_t)ti.h * p.T + tok] = lse;
-      }
-      ptx::mbar_arrive(&s.task_empty[slot]);
-      g += n;
-    }
+    const int wg = (warp >> 2) - 1;  // 0..3: (pipeline, column half)
+    const int pipe = wg >> 1;
+    run_softmax(p, sm.pipe[pipe], sm.tmem_base + 256u * pipe, wg & 1);
   }
 
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(s.tmem_base, TMEM_COLS);
+    ptx::tmem_dealloc(sm.tmem_base, TMEM_COLS);
   }
 }
 

@@ -121,15 +121,13 @@ static bsa_status_t check_device(size_t attn_smem, int *num_sms, int *per_sm = n
     di.smem_per_sm = smem_sm;
     di.smem_reserved = smem_res;
     if (di.state == 1) {
-      // The softmax warpgroup raises its registers with setmaxnreg.inc, drawing on what the
+      // The softmax warpgroups raise their registers with setmaxnreg.inc, drawing on what the
       // CTA was launched with; that only completes if the launch allocation covers the
       // whole split, so refuse to launch a build where it does not.
       cudaFuncAttributes fa;
       if (cudaFuncGetAttributes(&fa, attn::bsa_attention_kernel) != cudaSuccess)
         return BSA_ERR_CUDA;
-      if (fa.numRegs * attn::NTHREADS <
-          4 * 32 * attn::CTRL_REGS + 4 * 32 * attn::SOFTMAX_REGS)
-        di.state = 2;
+      if (fa.numRegs * attn::NTHREADS < attn::SPLIT_REGS) di.state = 2;
     }
   }
   if (di.state != 1) return BSA_ERR_UNSUPPORTED;
@@ -141,11 +139,7 @@ static bsa_status_t check_device(size_t attn_smem, int *num_sms, int *per_sm = n
     di.smem_attr = attn_smem;
   }
   if (num_sms) *num_sms = di.num_sms;
-  if (per_sm) {
-    // the kernel is built for two resident CTAs per SM (registers, TMEM); shared memory decides
-    const size_t per_block = attn_smem + (size_t)di.smem_reserved;
-    *per_sm = (2 * per_block <= (size_t)di.smem_per_sm) ? 2 : 1;
-  }
+  if (per_sm) *per_sm = 1;  // one CTA per SM: it holds the SM's registers and all of TMEM
   return BSA_OK;
 }
 
@@ -301,7 +295,7 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
     if (!encode_map(&tk, k_pages, 4, gd, gs, box)) return BSA_ERR_CUDA;
     if (!encode_map(&tv, v_pages, 4, gd, gs, box)) return BSA_ERR_CUDA;
   }
-  // persistent grid: as many CTAs as fit at once (two per SM when shared memory allows)
+  // persistent grid: one CTA per SM
   const long long grid = std::min<long long>(ntasks, (long long)per_sm * num_sms);
   if (cudaMemsetAsync(workspace, 0, sizeof(int), (cudaStream_t)stream) != cudaSuccess)
     return BSA_ERR_CUDA;
