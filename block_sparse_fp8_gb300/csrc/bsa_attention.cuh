@@ -11,9 +11,10 @@
 //                   coordinate, which fills zeros).
 //   MMA warp        one thread issues tcgen05.mma kind::f8f6f4: S(t+1) = Q K(t+1)^T as soon as
 //                   the softmax has read S(t), then O (+)= P(t) V(t).
-//   2 softmax       one warpgroup per half of a tile's 128 KV columns; a thread owns one query
-//   warpgroups      row of its half: scale, the row max (the two halves exchange theirs through
-//                   shared memory), P = 2^(x - m) at the fixed P-scale (exact zeros past the
+//   2 softmax       8 warps; warp (quarter q, sub-block u) owns rows 32q + 16u .. +15 of each
+//   warpgroups      tile, and in it lane i takes row 32q + 16u + i%16 and column half i/16
+//                   (tcgen05.ld shape 16x32bx2), so a row's two halves meet in one shuffle:
+//                   scale, the row max, P = 2^(x - m) at the fixed P-scale (exact zeros past the
 //                   causal edge and kv_len) rounded to e4m3 into a 128B-swizzled shared tile
 //                   (the A operand of the PV MMA), O rescaled in TMEM when the row max moves,
 //                   and the epilogue O * v_descale / l -> bf16, LSE -> fp32.
@@ -24,8 +25,6 @@
 // Method: hpc-ops Block-Sparse FP8 Attention (活跃 tile 列表; 固定 P-scale 量化技巧) and the
 // formula of Quant Block Sparse Attention (算子介绍).
 #pragma once
-
-#include <type_traits>
 
 #include "bsa_common.cuh"
 #include "ptx_sm103.cuh"
@@ -38,6 +37,8 @@ constexpr int NTHREADS = 640;        // 4 control warps + 2 pipelines x 2 softma
 constexpr int KSTAGES = 2;
 constexpr int VSTAGES = 2;
 constexpr int KDSTAGES = 2;
+constexpr int KD_STRIDE = TILE + 4;
+__host__ __device__ constexpr int kd_index(int token) { return token + (token >= 64 ? 4 : 0); }
 constexpr uint32_t TMEM_COLS = 512;  // per pipeline: S [0, 128), O [128, 256)
 constexpr bool POLY_EXP = false;     // part of exp2 on the FMA pipe (see exp2_poly2); measured slower
 constexpr int CTRL_REGS = 56;
@@ -58,8 +59,9 @@ struct __align__(1024) Pipe {
   uint8_t k[KSTAGES][TILE * HEAD_DIM];
   uint8_t v[VSTAGES][TILE * HEAD_DIM];
   uint8_t p[TILE * HEAD_DIM];
-  float kd[KDSTAGES][TILE];
-  float xbuf[2][2][TILE];  // [exchange parity][column half][row]: row max / row sum exchange
+  // per-token K descales of a tile; the second 64 tokens start 16 bytes late so that the two
+  // column halves of a warp read different banks
+  float kd[KDSTAGES][KD_STRIDE];
   TaskInfo info[2];
   uint32_t bitmap[KB_MAX / 32];
   uint64_t task_full[2], task_empty[2];
@@ -68,7 +70,6 @@ struct __align__(1024) Pipe {
   uint64_t v_full[VSTAGES], v_empty[VSTAGES];
   uint64_t kd_full[KDSTAGES], kd_empty[KDSTAGES];
   uint64_t s_full, s_empty, p_full, o_done, o_empty, drain;
-  uint64_t xchg[4];  // one per 32-row quarter: the two column halves of those rows meet here
   int abort_flag;
 };
 
@@ -230,7 +231,7 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               if (i < npg && pgs[i] < p.num_pages)
-                ptx::bulk_load(&s.kd[ds][i * p.ps],
+                ptx::bulk_load(&s.kd[ds][kd_index(i * p.ps)],
                                p.k_descale + ((size_t)pgs[i] * p.N2 + g_kv) * p.ps,
                                (uint32_t)(p.ps * 4), &s.kd_full[ds]);
           }
@@ -372,29 +373,17 @@ __device__ __forceinline__ void run_mma(const Params &p, Pipe &s, uint32_t tmem)
 }
 
 // ===================================================================================== softmax
-// Publishes `v` for row r, meets the other column half of the same 32 rows on xchg[quad] and
-// returns its value.  The two halves alternate between two buffers; neither can run two
-// exchanges ahead of the other, since each exchange needs both halves' arrivals.
-__device__ __forceinline__ bool exchange(const Params &p, Pipe &s, int quad, int half, int r,
-                                         uint32_t &xc, float v, float &other) {
-  s.xbuf[xc & 1][half][r] = v;
-  ptx::mbar_arrive(&s.xchg[quad]);
-  if (!wait_bar_warp(p, s, &s.xchg[quad], xc & 1)) return false;
-  other = s.xbuf[xc & 1][half ^ 1][r];
-  ++xc;
-  return true;
-}
-
-// Thread (half, r) owns columns [64*half, 64*half + 64) of row r of every tile.
-__device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t tmem, int half) {
+// Thread (row r, half h) owns columns [64h, 64h + 64) of row r of every tile; `sub` selects
+// which 16 rows of each 32-row TMEM quarter this warpgroup takes.
+__device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t tmem, int sub) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;  // a warp may touch TMEM lanes 32*(warp%4) .. +31
-  const int r = quad * 32 + lane;
+  const int r = quad * 32 + sub * 16 + (lane & 15);
+  const int half = lane >> 4;
   const int col0 = half * 64;
-  const uint32_t tS = tmem + ((uint32_t)(quad * 32) << 16) + col0;
+  const uint32_t tS = tmem + ((uint32_t)(quad * 32 + sub * 16) << 16);
   const uint32_t tO = tS + 128;
   uint8_t *prow = s.p + (r >> 3) * 1024 + (r & 7) * 128;
-  uint32_t xc = 0;
   int k = 0;
   uint32_t g = 0;
   for (;; ++k) {
@@ -416,9 +405,11 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
       causal_lim = qt * TILE + r + (ti.kv_len - q_len);
     }
     const bool neg_scale = row_scale < 0.f;
-    const float rs_abs = fabsf(row_scale);
+    // |scale| floored at 1e-30: a row whose descale is 0 then has logits of about 1e-23 in
+    // place of exact zeros (the same P in fp32), and a hidden key's -inf stays -inf
+    const float rs_abs = fmaxf(fabsf(row_scale), 1e-30f);
     const uint64_t rs2 = ptx::pk(rs_abs, rs_abs);
-    float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+    float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum (same m in both)
     bool ok = true;
     for (int t = 0; t < n; ++t) {
       const uint32_t gt = g + t;
@@ -428,8 +419,8 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
       }
       ptx::tc_fence_after();
       uint32_t x[2][32];
-      ptx::tmem_ld32(tS, x[0]);
-      ptx::tmem_ld32(tS + 32, x[1]);
+      ptx::tmem_ld16x2_32<64>(tS, x[0]);
+      ptx::tmem_ld16x2_32<64>(tS + 32, x[1]);
       ptx::tmem_ld_wait(x[0]);
       ptx::reg_fence(x[1]);
       ptx::tc_fence_before();
@@ -441,7 +432,7 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
           ok = false;
           break;
         }
-        const ulonglong2 *kd4 = reinterpret_cast<const ulonglong2 *>(&s.kd[ds][col0]);
+        const ulonglong2 *kd4 = reinterpret_cast<const ulonglong2 *>(&s.kd[ds][kd_index(col0)]);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -467,86 +458,66 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[c][j] ^= 0x80000000u;
       }
-      // visible keys of this half of the tile (the rest lies past the causal edge or
-      // kv_len); only the task's last two tiles can have any hidden key
-      int lim = 64;
+      // hidden keys (past the causal edge or kv_len) take the logit -inf: they neither raise
+      // the max nor add to P.  Only the task's last two tiles can hold any.
       if (t + 2 >= n) {
         const int tile = (t + 2 == n) ? ti.tail0 : ti.tail1;
-        lim = ti.kv_len - tile * TILE;
+        int lim = ti.kv_len - tile * TILE;  // visible keys of the tile
         if (p.causal) lim = min(lim, causal_lim - tile * TILE + 1);
-        lim -= col0;
-      }
-      float alpha = 1.f;
-      uint32_t packed[16];  // this half of the row of P as e4m3, 4 keys per word
-      // one specialisation per tile kind: the unmasked one carries no per-key selects
-      auto tile_body = [&](auto masked_tag) -> bool {
-        constexpr bool MASKED = decltype(masked_tag)::value;
-        if constexpr (MASKED) {
+        lim -= col0;                        // ... of this thread's half
+        if (__any_sync(0xffffffffu, lim < 64)) {
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (c * 32 + j >= lim) x[c][j] = f2u(-INFINITY);
         }
-        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+      }
+      float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        a0 = ptx::max3(a0, u2f(x[0][j]), u2f(x[0][j + 1]));
+        a1 = ptx::max3(a1, u2f(x[0][j + 2]), u2f(x[0][j + 3]));
+        a2 = ptx::max3(a2, u2f(x[1][j]), u2f(x[1][j + 1]));
+        a3 = ptx::max3(a3, u2f(x[1][j + 2]), u2f(x[1][j + 3]));
+      }
+      float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the row's other half
+      // largest scaled logit of the tile so far (log2 units); -inf while every key is hidden
+      const float m_new = fmaxf(m, mx * rs_abs);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ptx::ex2_approx(m - m_use);
+      const uint64_t b2 = ptx::pk(p.log2_pscale - m_use, p.log2_pscale - m_use);
+      uint32_t packed[16];          // this half of the row of P as e4m3, 4 keys per word
+      uint64_t acc0 = 0, acc1 = 0;  // packed partial sums (the 0.0f bit pattern is 0)
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-          a0 = ptx::max3(a0, u2f(x[0][j]), u2f(x[0][j + 1]));
-          a1 = ptx::max3(a1, u2f(x[0][j + 2]), u2f(x[0][j + 3]));
-          a2 = ptx::max3(a2, u2f(x[1][j]), u2f(x[1][j + 1]));
-          a3 = ptx::max3(a3, u2f(x[1][j + 2]), u2f(x[1][j + 3]));
-        }
-        float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-        float mx_other = -INFINITY;
-        if (!exchange(p, s, quad, half, r, xc, mx, mx_other)) return false;
-        mx = fmaxf(mx, mx_other);  // the same value in both halves
-        // largest scaled logit of the tile (log2 units); -inf when every key is hidden
-        const float tmax = mx == -INFINITY ? -INFINITY : mx * rs_abs;
-        const float m_new = fmaxf(m, tmax);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        alpha = ptx::ex2_approx(m - m_use);
-        const uint64_t b2 = ptx::pk(p.log2_pscale - m_use, p.log2_pscale - m_use);
-        uint64_t acc0 = 0, acc1 = 0;  // packed partial sums (the 0.0f bit pattern is 0)
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            float e0, e1, e2, e3;
-            ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j]), u2f(x[c][j + 1])), rs2, b2), e0, e1);
-            ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j + 2]), u2f(x[c][j + 3])), rs2, b2), e2, e3);
-            if constexpr (MASKED) {  // hidden keys: exponent -inf (also when the scale is 0)
-              if (c * 32 + j + 0 >= lim) e0 = -INFINITY;
-              if (c * 32 + j + 1 >= lim) e1 = -INFINITY;
-              if (c * 32 + j + 2 >= lim) e2 = -INFINITY;
-              if (c * 32 + j + 3 >= lim) e3 = -INFINITY;
-            }
-            float p0, p1, p2, p3;
-            if (POLY_EXP && p.poly_exp && ((c * 8 + (j >> 2)) % 3) == 2) {
-              ptx::exp2_poly2(e0, e1, p0, p1);
-              ptx::exp2_poly2(e2, e3, p2, p3);
-            } else {
-              p0 = ptx::ex2_approx(e0);
-              p1 = ptx::ex2_approx(e1);
-              p2 = ptx::ex2_approx(e2);
-              p3 = ptx::ex2_approx(e3);
-            }
-            acc0 = ptx::add2(acc0, ptx::pk(p0, p1));
-            acc1 = ptx::add2(acc1, ptx::pk(p2, p3));
-            packed[(c * 32 + j) >> 2] =
-                (uint32_t)ptx::cvt_e4m3x2(p0, p1) | ((uint32_t)ptx::cvt_e4m3x2(p2, p3) << 16);
+          float e0, e1, e2, e3;
+          ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j]), u2f(x[c][j + 1])), rs2, b2), e0, e1);
+          ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j + 2]), u2f(x[c][j + 3])), rs2, b2), e2, e3);
+          float p0, p1, p2, p3;
+          if (POLY_EXP && p.poly_exp && ((c * 8 + (j >> 2)) % 3) == 2) {
+            ptx::exp2_poly2(e0, e1, p0, p1);
+            ptx::exp2_poly2(e2, e3, p2, p3);
+          } else {
+            p0 = ptx::ex2_approx(e0);
+            p1 = ptx::ex2_approx(e1);
+            p2 = ptx::ex2_approx(e2);
+            p3 = ptx::ex2_approx(e3);
           }
+          acc0 = ptx::add2(acc0, ptx::pk(p0, p1));
+          acc1 = ptx::add2(acc1, ptx::pk(p2, p3));
+          packed[(c * 32 + j) >> 2] =
+              (uint32_t)ptx::cvt_e4m3x2(p0, p1) | ((uint32_t)ptx::cvt_e4m3x2(p2, p3) << 16);
+        }
+      {
         float s0, s1, s2, s3;
         ptx::upk(acc0, s0, s1);
         ptx::upk(acc1, s2, s3);
         l = alpha * l + ((s0 + s1) + (s2 + s3));
         m = m_new;
-        return true;
-      };
-      const bool body_ok =
-          (lim < 64) ? tile_body(std::true_type{}) : tile_body(std::false_type{});
-      if (!body_ok) {
-        ok = false;
-        break;
       }
       if (t > 0) {
         // PV(t-1) done: the P tile may be overwritten and O is stable for the rescale
@@ -565,23 +536,21 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
             make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
       ptx::fence_proxy_async_smem();
       if (t > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
-        // O *= alpha on this half's 64 columns of the warp's rows
+        // O *= alpha on this thread's 64 columns, 32 at a time
         const uint64_t a2 = ptx::pk(alpha, alpha);
-        uint32_t o[2][32];
-        ptx::tmem_ld32(tO, o[0]);
-        ptx::tmem_ld32(tO + 32, o[1]);
-        ptx::tmem_ld_wait(o[0]);
-        ptx::reg_fence(o[1]);
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 2; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld16x2_32<64>(tO + c * 32, o);
+          ptx::tmem_ld_wait(o);
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             float a, b3;
-            ptx::upk(ptx::mul2(ptx::pk(u2f(o[c][j]), u2f(o[c][j + 1])), a2), a, b3);
-            o[c][j] = f2u(a);
-            o[c][j + 1] = f2u(b3);
+            ptx::upk(ptx::mul2(ptx::pk(u2f(o[j]), u2f(o[j + 1])), a2), a, b3);
+            o[j] = f2u(a);
+            o[j + 1] = f2u(b3);
           }
-          ptx::tmem_st32(tO + c * 32, o[c]);
+          ptx::tmem_st16x2_32<64>(tO + c * 32, o);
         }
         ptx::tmem_st_wait();
       }
@@ -595,9 +564,7 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
     const bool row_ok = r < min(TILE, ti.q_len - qt * TILE);
     const int tok = ti.q0 + qt * TILE + r;
     const int g_kv = h / p.G;
-    float l_other = 0.f;
-    if (!exchange(p, s, quad, half, r, xc, l, l_other)) break;
-    const float l_row = l + l_other;  // both halves kept the same running max
+    const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);  // both halves share m
     if (n > 0) {
       if (!wait_bar_warp(p, s, &s.o_done, (g + n - 1) & 1)) break;
       ptx::tc_fence_after();
@@ -613,7 +580,7 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
     for (int c = 0; c < 2; ++c) {
       uint32_t o[32];
       if (n > 0) {
-        ptx::tmem_ld32(tO + c * 32, o);
+        ptx::tmem_ld16x2_32<64>(tO + c * 32, o);
         ptx::tmem_ld_wait(o);
       } else {
 #pragma unroll
@@ -682,7 +649,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ptx::mbar_init(&s.o_done, 1);
     ptx::mbar_init(&s.o_empty, 256);
     ptx::mbar_init(&s.drain, 1);
-    for (int i = 0; i < 4; ++i) ptx::mbar_init(&s.xchg[i], 64);  // two warps, one per half
     s.abort_flag = 0;
     ptx::fence_mbarrier_init();
     if (threadIdx.x == 0) {
@@ -711,7 +677,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     ptx::regs_inc<SOFTMAX_REGS>();
-    const int wg = (warp >> 2) - 1;  // 0..3: (pipeline, column half)
+    const int wg = (warp >> 2) - 1;  // 0..3: (pipeline, row sub-block)
     const int pipe = wg >> 1;
     run_softmax(p, sm.pipe[pipe], sm.tmem_base + 256u * pipe, wg & 1);
   }
