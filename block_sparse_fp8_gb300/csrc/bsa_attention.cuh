@@ -618,8 +618,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                          const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
+  // 1024-byte alignment (128B-swizzled tiles) by pointer arithmetic on smem_raw, so that the
+  // compiler still knows every access through `base` is a shared-memory access
+  uint8_t *base = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   Smem &sm = *reinterpret_cast<Smem *>(base);
   const int warp = threadIdx.x >> 5;
 
