@@ -106,10 +106,18 @@ __device__ __forceinline__ bool wait_bar(const Params &p, Pipe &s, uint64_t *bar
   }
 }
 
+// The softmax warps' waits after a first failed test, out of line so that their hot path
+// carries only the test (the smaller loop body measurably helps the softmax).
+__device__ __noinline__ bool wait_bar_warp_slow(const Params &p, Pipe &s, uint64_t *bar,
+                                                uint32_t parity) {
+  return __all_sync(0xffffffffu, wait_bar(p, s, bar, parity));
+}
+
 // Warp-uniform version for code followed by warp-collective instructions.
 __device__ __forceinline__ bool wait_bar_warp(const Params &p, Pipe &s, uint64_t *bar,
                                               uint32_t parity) {
-  return __all_sync(0xffffffffu, wait_bar(p, s, bar, parity));
+  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+  return wait_bar_warp_slow(p, s, bar, parity);
 }
 
 // Bounded wait that ignores the abort flag (used to let in-flight async work land).
@@ -574,8 +582,18 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
     const float vd = p.v_per_head ? p.v_descale[g_kv] : p.v_descale[0];
     const float osc = seen ? vd / l_row : 0.f;
     const uint64_t osc2 = ptx::pk(osc, osc);
-    uint4 *orow =
-        reinterpret_cast<uint4 *>(p.out + ((size_t)tok * p.N1 + h) * HEAD_DIM + col0);
+    // O goes out through this warp's 16 rows of the P tile (PV has finished reading them):
+    // each 32-column round is staged row-wise and copied out so that a store instruction
+    // writes whole 64-byte row segments instead of 16 bytes from each of 32 rows.  Staged
+    // row i holds its two 64-byte segments as chunks 0-3 and 4-7, chunk c at position
+    // c ^ (i % 8) so that both the staging and the copy-out touch every bank once per 128 B.
+    const int r0 = quad * 32 + sub * 16;
+    uint8_t *stage = s.p + r0 * 128;
+    const int i = lane & 15;
+    const int rows_valid = min(TILE, ti.q_len - qt * TILE);
+    uint8_t *orow0 = reinterpret_cast<uint8_t *>(p.out) +
+                     ((size_t)(ti.q0 + qt * TILE + r0) * p.N1 + h) * (HEAD_DIM * 2);
+    const size_t row_bytes = (size_t)p.N1 * HEAD_DIM * 2;
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
       uint32_t o[32];
@@ -594,11 +612,20 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
         __nv_bfloat162 v2 = __floats2bfloat162_rn(a, b3);
         w[j] = *reinterpret_cast<uint32_t *>(&v2);
       }
-      if (row_ok) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          orow[c * 4 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(stage + i * 128 + (((4 * half + q) ^ (i & 7)) << 4)) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int i2 = kk * 4 + (lane >> 3), c8 = lane & 7;
+        const uint4 v = *reinterpret_cast<const uint4 *>(stage + i2 * 128 + ((c8 ^ (i2 & 7)) << 4));
+        if (r0 + i2 < rows_valid)
+          *reinterpret_cast<uint4 *>(orow0 + i2 * row_bytes + (c8 >> 2) * 128 + c * 64 +
+                                     (c8 & 3) * 16) = v;
       }
+      __syncwarp();
     }
     ptx::tc_fence_before();
     ptx::mbar_arrive(&s.o_empty);
