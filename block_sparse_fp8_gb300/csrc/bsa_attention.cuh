@@ -413,6 +413,7 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
       causal_lim = qt * TILE + r + (ti.kv_len - q_len);
     }
     const bool neg_scale = row_scale < 0.f;
+    const bool any_neg = __any_sync(0xffffffffu, neg_scale);
     // |scale| floored at 1e-30: a row whose descale is 0 then has logits of about 1e-23 in
     // place of exact zeros (the same P in fp32), and a hidden key's -inf stays -inf
     const float rs_abs = fmaxf(fabsf(row_scale), 1e-30f);
@@ -460,7 +461,7 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
       }
       // a negative scale (never produced by amax/448 descales, but legal) is folded into the
       // values so that one row-max path serves every row
-      if (__any_sync(0xffffffffu, neg_scale) && neg_scale) {
+      if (any_neg && neg_scale) {
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -544,21 +545,23 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
             make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
       ptx::fence_proxy_async_smem();
       if (t > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
-        // O *= alpha on this thread's 64 columns, 32 at a time
+        // O *= alpha on this thread's 64 columns
         const uint64_t a2 = ptx::pk(alpha, alpha);
-#pragma unroll 1
+        uint32_t o[2][32];
+        ptx::tmem_ld16x2_32<64>(tO, o[0]);
+        ptx::tmem_ld16x2_32<64>(tO + 32, o[1]);
+        ptx::tmem_ld_wait(o[0]);
+        ptx::reg_fence(o[1]);
+#pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t o[32];
-          ptx::tmem_ld16x2_32<64>(tO + c * 32, o);
-          ptx::tmem_ld_wait(o);
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             float a, b3;
-            ptx::upk(ptx::mul2(ptx::pk(u2f(o[j]), u2f(o[j + 1])), a2), a, b3);
-            o[j] = f2u(a);
-            o[j + 1] = f2u(b3);
+            ptx::upk(ptx::mul2(ptx::pk(u2f(o[c][j]), u2f(o[c][j + 1])), a2), a, b3);
+            o[c][j] = f2u(a);
+            o[c][j + 1] = f2u(b3);
           }
-          ptx::tmem_st16x2_32<64>(tO + c * 32, o);
+          ptx::tmem_st16x2_32<64>(tO + c * 32, o[c]);
         }
         ptx::tmem_st_wait();
       }
