@@ -518,8 +518,7 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
           }
           acc0 = ptx::add2(acc0, ptx::pk(p0, p1));
           acc1 = ptx::add2(acc1, ptx::pk(p2, p3));
-          packed[(c * 32 + j) >> 2] =
-              (uint32_t)ptx::cvt_e4m3x2(p0, p1) | ((uint32_t)ptx::cvt_e4m3x2(p2, p3) << 16);
+          packed[(c * 32 + j) >> 2] = ptx::cvt_e4m3x4(p0, p1, p2, p3);
         }
       {
         float s0, s1, s2, s3;

@@ -299,10 +299,17 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Two fp32 -> two e4m3 (round to nearest even, saturate to +-448), `lo` in the low byte.
-__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+// Four fp32 -> four e4m3 (round to nearest even, saturate to +-448) in one word, p0 in the
+// low byte; the two halves are assembled in PTX, which lets the second conversion merge into
+// the first's register.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float p0, float p1, float p2, float p3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(p0), "f"(p1), "f"(p2), "f"(p3));
   return r;
 }
 
