@@ -428,8 +428,7 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
       }
       ptx::tc_fence_after();
       uint32_t x[2][32];
-      ptx::tmem_ld16x2_32<64>(tS, x[0]);
-      ptx::tmem_ld16x2_32<64>(tS + 32, x[1]);
+      ptx::tmem_ld16x2_64<64>(tS, x[0], x[1]);
       ptx::tmem_ld_wait(x[0]);
       ptx::reg_fence(x[1]);
       ptx::tc_fence_before();
