@@ -17,6 +17,7 @@ path has no data exchange), timed between barriers, max over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -65,6 +66,31 @@ def peaks():
         return pk, "measured"
     except (OSError, ValueError):
         return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
+
+
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "bsa_attention_kernel__dram_traffic.json")
+KERNEL_SOURCES = ("bsa_attention.cuh", "bsa_common.cuh", "ptx_sm103.cuh", "bsa_fp8.cu")
+
+
+def kernel_sources_digest():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "block_sparse_fp8_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload):
+    """DRAM bytes (read + write) per launch of the attention kernel on `workload`, from the
+    committed ncu record; None when the record was taken on other kernel sources."""
+    try:
+        with open(TRAFFIC_RECORD) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_sources_sha256") != kernel_sources_digest():
+        return None
+    return rec.get("dram_bytes_per_launch", {}).get(workload)
 
 
 def config_of(case, name, tiles, flops):
@@ -344,7 +370,8 @@ def run_ours(args, rank, world):
         "ms_per_call": {"mean": ms, "median": statistics.median(per), "min": min(per)},
         "wall_ms_per_step_incl_flush": wall * 1e3 / args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak,
-                     "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+                     "traffic": measured_traffic(args.workload) if args.batch == 0 else None,
                      "peak_source": f"{src}: bf16 {'burst' if src == 'measured' else ''} "
                                     f"{pk.get('bf16_tflops')} TFLOP/s x {FP8_PER_BF16} "
                                     f"(nominal fp8/bf16 ratio)",
