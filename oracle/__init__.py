@@ -7,7 +7,9 @@ does.  The C source, ``bsa_oracle.c``, restates the formula of "Quant Block Spar
 FP8 Attention" (section 固定 P-scale 量化技巧); its header lists the readings it takes.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py`` (brute-force
-dense attention, closed forms, invariants, the exhaustive e4m3 table).
+dense attention, closed forms, invariants, the exhaustive e4m3 table; the quantise and
+KV-append step against numpy fp32 arithmetic with PyTorch's e4m3 cast and hand-derived
+codes).
 """
 from __future__ import annotations
 
@@ -90,6 +92,11 @@ def load(path: str | None = None):
                                           ctypes.c_void_p, ctypes.c_long, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_quantize_rows.restype = None
+    lib.oracle_quantize_rows.argtypes = [ctypes.c_void_p, ctypes.c_long, ctypes.c_void_p,
+                                         ctypes.c_void_p]
+    lib.oracle_append_kv.restype = ctypes.c_int
+    lib.oracle_append_kv.argtypes = [ctypes.c_int] * 7 + [ctypes.c_void_p] * 10
     if path is None:
         _lib = lib
     return lib
@@ -142,6 +149,42 @@ class Oracle:
         rows = np.stack([tok.ravel(), h.ravel()], axis=1)
         o, lse, err = self.rows(rows, mode, nthreads)
         return o.reshape(c.T, c.N1, 128), lse.reshape(c.T, c.N1).T.copy(), err
+
+
+def quantize_rows(x_bf16: np.ndarray, lib=None):
+    """x_bf16: uint16 bf16 bit patterns [..., 128].  Returns (codes uint8 [..., 128], descale
+    float32 [...]): per row descale = amax/448 (1 for a zero row), code = e4m3(x / descale)."""
+    lib = lib if lib is not None else load()
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    assert x.shape[-1] == 128
+    rows = x.size // 128
+    codes = np.zeros(x.shape, dtype=np.uint8)
+    desc = np.zeros(x.shape[:-1], dtype=np.float32)
+    lib.oracle_quantize_rows(_ptr(x), rows, _ptr(codes), _ptr(desc))
+    return codes, desc
+
+
+def append_kv(k_new, v_new, cu_new, cache_len, block_table, k_pages, v_pages, k_descale,
+              k_scale_kind, v_scale_kind, k_scale=None, v_scale=None, lib=None):
+    """Writes bf16 K/V tokens [T_new, N2, 128] (uint16 bit patterns) into copies of the paged
+    cache arrays.  Returns (k_pages, v_pages, k_descale, err)."""
+    lib = lib if lib is not None else load()
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    cu_new = np.ascontiguousarray(cu_new, dtype=np.int32)
+    cache_len = np.ascontiguousarray(cache_len, dtype=np.int32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    kp = np.array(k_pages, dtype=np.uint8, copy=True)
+    vp = np.array(v_pages, dtype=np.uint8, copy=True)
+    kd = np.array(k_descale, dtype=np.float32, copy=True)
+    ks = np.ascontiguousarray(np.atleast_1d(k_scale if k_scale is not None else 1.0), dtype=np.float32)
+    vs = np.ascontiguousarray(np.atleast_1d(v_scale if v_scale is not None else 1.0), dtype=np.float32)
+    P, N2, ps, D = kp.shape
+    B = cu_new.size - 1
+    err = lib.oracle_append_kv(B, N2, ps, P, bt.shape[1], int(k_scale_kind), int(v_scale_kind),
+                               _ptr(k_new), _ptr(v_new), _ptr(cu_new), _ptr(cache_len), _ptr(bt),
+                               _ptr(ks), _ptr(vs), _ptr(kp), _ptr(vp), _ptr(kd))
+    return kp, vp, kd, err
 
 
 def e4m3_decode(code: int) -> float:

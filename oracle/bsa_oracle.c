@@ -370,3 +370,87 @@ int oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------------------
+ * Quantisation into the attention inputs (the step before the attention call).
+ *
+ * The FlashMLA page (section 量化 / 解量化的源码实现) states the rule for one 128-element
+ * tile: the scale is the tile's largest absolute value over 448 (the largest finite e4m3)
+ * and the stored value is e4m3(x / scale).  The attention pages give Q per token per head,
+ * K per token per head (or per tensor) and V per head (or per tensor) descales, i.e. the
+ * same rule applied to each 128-element row of Q and K.  Readings: no rounding of the scale
+ * to a power of two (that step belongs to FlashMLA's own cache format); an all-zero row gets
+ * descale 1 and zero codes; both divisions are fp32 divisions (the precision of the inputs'
+ * consumers); e4m3 rounds to nearest even and saturates (oracle_e4m3_encode).
+ * ------------------------------------------------------------------------------------ */
+static float bf16_value(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* One row of 128 bf16 values -> 128 codes; returns the row's descale. */
+static float quantize_row(const uint16_t *x, uint8_t *codes) {
+  float amax = 0.0f;
+  for (int i = 0; i < HEAD_DIM; ++i) {
+    float a = fabsf(bf16_value(x[i]));
+    if (a > amax) amax = a;
+  }
+  float descale = amax > 0.0f ? amax / 448.0f : 1.0f;
+  for (int i = 0; i < HEAD_DIM; ++i) {
+    float v = bf16_value(x[i]) / descale;
+    codes[i] = oracle_e4m3_encode((double)v);
+  }
+  return descale;
+}
+
+/* x [rows, 128] bf16 -> codes [rows, 128] e4m3, descale [rows] (Q [T, N1, 128] gives the
+ * q_descale layout [T, N1] directly). */
+void oracle_quantize_rows(const uint16_t *x, long rows, uint8_t *codes, float *descale) {
+  for (long r = 0; r < rows; ++r)
+    descale[r] = quantize_row(x + r * HEAD_DIM, codes + r * HEAD_DIM);
+}
+
+/* Writes new K/V tokens into the paged cache.  Token i of sequence b (rows cu_new[b] + i of
+ * k_new / v_new [T_new, N2, 128] bf16) lands at logical position pos = cache_len[b] + i, i.e.
+ * page block_table[b, pos / page_size], slot pos % page_size of [P, N2, page_size, 128].
+ * K: with SCALE_PER_TOKEN_HEAD each (token, head) row is quantised as above and its descale
+ * stored in k_descale [P, N2, page_size]; with SCALE_PER_TENSOR the codes are e4m3(x / k_scale)
+ * with the caller's k_scale.  V: e4m3(x / v_scale[head]) (SCALE_PER_HEAD) or / v_scale[0].
+ * A token whose page is missing or outside [0, num_pages) is skipped and reported. */
+int oracle_append_kv(int B, int N2, int page_size, int num_pages, int max_pages_per_seq,
+                     int k_scale_kind, int v_scale_kind, const uint16_t *k_new,
+                     const uint16_t *v_new, const int *cu_new, const int *cache_len,
+                     const int *block_table, const float *k_scale, const float *v_scale,
+                     uint8_t *k_pages, uint8_t *v_pages, float *k_descale) {
+  int err = 0;
+  for (int b = 0; b < B; ++b) {
+    int n = cu_new[b + 1] - cu_new[b];
+    for (int i = 0; i < n; ++i) {
+      long pos = (long)cache_len[b] + i;
+      long lp = pos / page_size;
+      int slot = (int)(pos % page_size);
+      int pg = lp < max_pages_per_seq ? block_table[(size_t)b * max_pages_per_seq + lp] : -1;
+      if (pg < 0 || pg >= num_pages) {
+        err |= ORACLE_BAD_PAGE;
+        continue;
+      }
+      for (int g = 0; g < N2; ++g) {
+        size_t src = ((size_t)(cu_new[b] + i) * N2 + g) * HEAD_DIM;
+        size_t row = ((size_t)pg * N2 + g) * page_size + slot;
+        if (k_scale_kind == SCALE_PER_TOKEN_HEAD) {
+          k_descale[row] = quantize_row(k_new + src, k_pages + row * HEAD_DIM);
+        } else {
+          for (int e = 0; e < HEAD_DIM; ++e)
+            k_pages[row * HEAD_DIM + e] =
+                oracle_e4m3_encode((double)(bf16_value(k_new[src + e]) / k_scale[0]));
+        }
+        float vs = v_scale_kind == SCALE_PER_HEAD ? v_scale[g] : v_scale[0];
+        for (int e = 0; e < HEAD_DIM; ++e)
+          v_pages[row * HEAD_DIM + e] = oracle_e4m3_encode((double)(bf16_value(v_new[src + e]) / vs));
+      }
+    }
+  }
+  return err;
+}

@@ -508,4 +508,140 @@ def pin_pemu_near_exact(lib):
     assert np.all(np.abs(l2 - l) <= 2.5e-5 + 0.005 * np.abs(l))
 
 
+# ----------------------------------------------------------------------------------------
+# quantisation into the attention inputs (FlashMLA page, 量化 / 解量化的源码实现: scale =
+# amax / 448, stored value e4m3(x / scale); readings in oracle/bsa_oracle.c)
+# ----------------------------------------------------------------------------------------
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even fp32 -> bf16 bit patterns (PyTorch's cast)."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def torch_quantize_rows(xb: np.ndarray):
+    """Independent restatement with numpy fp32 arithmetic and PyTorch's e4m3 cast."""
+    x = bf16_bits_to_f32(xb)
+    amax = np.abs(x).max(axis=-1)
+    d = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32), np.float32(1.0))
+    q = np.clip((x / d[..., None]).astype(np.float32), -448.0, 448.0).astype(np.float32)
+    codes = torch.from_numpy(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return codes, d.astype(np.float32)
+
+
+def _quant_rows_fixture():
+    rng = np.random.default_rng(1234)
+    x = rng.standard_normal((37, 128)).astype(np.float32)
+    x[3] = 0.0                                       # zero row -> descale 1, zero codes
+    x[5] *= 1e-4                                     # small values: subnormal e4m3 codes
+    x[6, 17] = 3.0e4                                 # one large outlier
+    x[7] = np.linspace(-1000.0, 1000.0, 128)         # codes spanning the whole range
+    x[8] *= 2.0 ** -20
+    return f32_to_bf16_bits(x)
+
+
+def pin_quantize_vs_torch_cast(lib):
+    xb = _quant_rows_fixture()
+    codes, desc = O.quantize_rows(xb, lib=lib)
+    t_codes, t_desc = torch_quantize_rows(xb)
+    assert np.array_equal(desc.view(np.uint32), t_desc.view(np.uint32)), "descales differ"
+    assert np.array_equal(codes, t_codes), f"{int((codes != t_codes).sum())} codes differ"
+
+
+def pin_quantize_closed_forms(lib):
+    vals = np.zeros((4, 128), dtype=np.float32)
+    vals[0, :5] = [448.0, -448.0, 0.5, -2.0 ** -6, 2.0 ** -9]   # amax 448 -> descale 1
+    vals[2, :3] = [896.0, 448.0, -1.0]                           # amax 896 -> descale 2
+    vals[3] = vals[0] * 2.0 ** 40                                # scaled copy of row 0
+    codes, desc = O.quantize_rows(f32_to_bf16_bits(vals), lib=lib)
+    assert desc[0] == 1.0 and desc[1] == 1.0 and desc[2] == 2.0 and desc[3] == 2.0 ** 40
+    assert list(codes[0, :5]) == [0x7E, 0xFE, 0x30, 0x88, 0x01]
+    assert not codes[0, 5:].any() and not codes[1].any()
+    assert list(codes[2, :3]) == [0x7E, 0x76, 0xB0]              # 448, 224, -0.5
+    assert np.array_equal(codes[3], codes[0])
+    # dequantisation error: half an e4m3 step (2^-4 relative) for normals, 2^-10 * descale
+    # (half the subnormal quantum) below
+    xb = _quant_rows_fixture()
+    codes, desc = O.quantize_rows(xb, lib=lib)
+    x = bf16_bits_to_f32(xb).astype(np.float64)
+    deq = torch_decode(codes) * desc[:, None].astype(np.float64)
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, desc[:, None] * 2.0 ** -10) * (1 + 1e-6)
+    assert np.all(np.abs(deq - x) <= bound)
+
+
+def _append_fixture(k_kind, v_kind):
+    rng = np.random.default_rng(99)
+    P, N2, ps = 9, 2, 4
+    L = 4
+    bt = np.full((2, L), -1, dtype=np.int32)
+    perm = rng.permutation(P)
+    bt[0, :3] = perm[:3]
+    bt[1, :4] = perm[3:7]
+    cache_len = np.array([5, 0], dtype=np.int32)
+    cu_new = np.array([0, 6, 13], dtype=np.int32)      # 6 new tokens for b=0, 7 for b=1
+    kx = rng.standard_normal((13, N2, 128)).astype(np.float32) * 3
+    vx = rng.standard_normal((13, N2, 128)).astype(np.float32)
+    kb, vb = f32_to_bf16_bits(kx), f32_to_bf16_bits(vx)
+    kp = np.full((P, N2, ps, 128), 0x55, dtype=np.uint8)
+    vp = np.full((P, N2, ps, 128), 0x55, dtype=np.uint8)
+    kd = np.full((P, N2, ps), -7.0, dtype=np.float32)
+    k_scale = np.array([0.02], dtype=np.float32)
+    v_scale = np.array([0.01, 0.005], dtype=np.float32) if v_kind == W.SCALE_PER_HEAD else \
+        np.array([0.01], dtype=np.float32)
+    return dict(kb=kb, vb=vb, cu_new=cu_new, cache_len=cache_len, bt=bt, kp=kp, vp=vp, kd=kd,
+                k_scale=k_scale, v_scale=v_scale, ps=ps)
+
+
+def _torch_codes(x, scale):
+    q = np.clip((x / scale).astype(np.float32), -448.0, 448.0).astype(np.float32)
+    return torch.from_numpy(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_append_kv_placement(lib):
+    for k_kind, v_kind in ((W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD),
+                           (W.SCALE_PER_TENSOR, W.SCALE_PER_TENSOR)):
+        f = _append_fixture(k_kind, v_kind)
+        kp, vp, kd, err = O.append_kv(f["kb"], f["vb"], f["cu_new"], f["cache_len"], f["bt"],
+                                      f["kp"], f["vp"], f["kd"], k_kind, v_kind,
+                                      f["k_scale"], f["v_scale"], lib=lib)
+        assert err == 0
+        ps = f["ps"]
+        written = np.zeros(kp.shape[:3], dtype=bool)
+        kx, vx = bf16_bits_to_f32(f["kb"]), bf16_bits_to_f32(f["vb"])
+        for b in range(2):
+            for i in range(f["cu_new"][b + 1] - f["cu_new"][b]):
+                tok = f["cu_new"][b] + i
+                pos = f["cache_len"][b] + i
+                pg = f["bt"][b, pos // ps]
+                slot = pos % ps
+                for g in range(2):
+                    written[pg, g, slot] = True
+                    if k_kind == W.SCALE_PER_TOKEN_HEAD:
+                        c, d = torch_quantize_rows(f["kb"][tok, g][None])
+                        assert np.array_equal(kp[pg, g, slot], c[0]) and kd[pg, g, slot] == d[0]
+                    else:
+                        assert np.array_equal(kp[pg, g, slot], _torch_codes(kx[tok, g], f["k_scale"][0]))
+                    vs = f["v_scale"][g] if v_kind == W.SCALE_PER_HEAD else f["v_scale"][0]
+                    assert np.array_equal(vp[pg, g, slot], _torch_codes(vx[tok, g], vs))
+        # every other slot is untouched
+        assert np.all(kp[~written] == 0x55) and np.all(vp[~written] == 0x55)
+        if k_kind == W.SCALE_PER_TOKEN_HEAD:
+            assert np.all(kd[~written] == -7.0)
+        else:
+            assert np.all(kd == -7.0)
+    # a missing page is reported and its tokens skipped
+    f = _append_fixture(W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD)
+    bt = f["bt"].copy()
+    bt[1, 1] = -1
+    kp, vp, kd, err = O.append_kv(f["kb"], f["vb"], f["cu_new"], f["cache_len"], bt, f["kp"],
+                                  f["vp"], f["kd"], W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD,
+                                  f["k_scale"], f["v_scale"], lib=lib)
+    assert err == O.ERR_BAD_PAGE
+    assert np.all(kp[f["bt"][1, 1]] == 0x55)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -43,6 +43,17 @@ MUTANTS = {
                               "(double)(float)(p * in->p_scale))) / in->p_scale;"),
     "pemu_exact_p_in_pv": ("tile_acc[k] += pq * oracle_e4m3_decode(vr[k]);",
                            "tile_acc[k] += p * in->p_scale * oracle_e4m3_decode(vr[k]);"),
+    "quant_wrong_max": ("float descale = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                        "float descale = amax > 0.0f ? amax / 240.0f : 1.0f;"),
+    "quant_zero_row_descale": ("float descale = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                               "float descale = amax > 0.0f ? amax / 448.0f : 0.0f;"),
+    "quant_multiply_by_descale": ("float v = bf16_value(x[i]) / descale;",
+                                  "float v = bf16_value(x[i]) * descale;"),
+    "append_ignores_cache_len": ("long pos = (long)cache_len[b] + i;", "long pos = i;"),
+    "append_slot_transposed": ("size_t row = ((size_t)pg * N2 + g) * page_size + slot;",
+                               "size_t row = ((size_t)g * num_pages + pg) * page_size + slot;"),
+    "append_v_scale_head0": ("float vs = v_scale_kind == SCALE_PER_HEAD ? v_scale[g] : v_scale[0];",
+                             "float vs = v_scale[0];"),
 }
 
 
