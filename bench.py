@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--op", choices=["prefill", "quantize"], default="prefill",
+                    help="prefill (the hot path, default) or the quantise step that feeds it: "
+                         "bf16 Q rows + K/V append of the workload's shapes")
     ap.add_argument("--batch", type=int, default=0,
                     help="keep only the first N sequences of the workload (profiling runs)")
     return ap.parse_args()
@@ -69,7 +72,8 @@ def peaks():
 
 
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "bsa_attention_kernel__dram_traffic.json")
-KERNEL_SOURCES = ("bsa_attention.cuh", "bsa_common.cuh", "ptx_sm103.cuh", "bsa_fp8.cu")
+# the attention kernel's device code (its launch shape is fixed: one 640-thread CTA per SM)
+KERNEL_SOURCES = ("bsa_attention.cuh", "bsa_common.cuh", "ptx_sm103.cuh")
 
 
 def kernel_sources_digest():
@@ -438,12 +442,123 @@ def run_reference(args, rank):
             "gpu_launches": 0}
 
 
+def run_quantize(args, rank, world):
+    """The quantise step at the workload's shapes: bsa_fp8_quantize_rows over Q [T, N1, 128]
+    bf16 and bsa_fp8_append_kv of all K/V tokens [T_kv, N2, 128] bf16 (per-token K, per-head
+    V) into fresh pages.  HBM-bound: value = algorithmic bytes / time."""
+    import torch
+
+    import block_sparse_fp8_gb300 as bsa
+    from block_sparse_fp8_gb300 import _build
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    if _build.needs_build():
+        if rank == 0:
+            _build.build()
+        if world > 1:
+            torch.distributed.barrier()
+    bsa.lib()
+    w = dict(W.WORKLOADS[args.workload])
+    q_lens, kv_lens, N1, N2, ps = w["q_lens"], w["kv_lens"], w["N1"], w["N2"], w["page_size"]
+    T, Tkv, B = sum(q_lens), sum(kv_lens), len(kv_lens)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + rank)
+    q = torch.randn((T, N1, 128), generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn((Tkv, N2, 128), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((Tkv, N2, 128), generator=g, device=dev).to(torch.bfloat16)
+    pages = [-(-kv // ps) for kv in kv_lens]
+    P, L = sum(pages), max(pages)
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(5)).to(torch.int32)
+    bt = torch.full((B, L), -1, dtype=torch.int32)
+    o = 0
+    for b, n in enumerate(pages):
+        bt[b, :n] = perm[o:o + n]
+        o += n
+    bt = bt.to(dev)
+    cu_new = torch.tensor([0] + list(np.cumsum(kv_lens)), dtype=torch.int32, device=dev)
+    cache_len = torch.zeros(B, dtype=torch.int32, device=dev)
+    k_pages = torch.zeros((P, N2, ps, 128), dtype=torch.uint8, device=dev)
+    v_pages = torch.zeros_like(k_pages)
+    k_desc = torch.zeros((P, N2, ps), dtype=torch.float32, device=dev)
+    v_scale = torch.full((N2,), 4.0 / 448.0, dtype=torch.float32, device=dev)
+    q8 = torch.empty((T, N1, 128), dtype=torch.uint8, device=dev)
+    qd = torch.empty((T, N1), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        bsa.quantize_rows(q, q8, qd)
+        bsa.append_kv(k, v, cu_new, cache_len, bt, k_pages, v_pages, k_descale=k_desc,
+                      v_scale=v_scale, dev_status=status)
+
+    # algorithmic bytes: bf16 in, e4m3 out, one fp32 descale per row (Q and K); block table
+    # and lengths are negligible
+    nbytes = T * N1 * (256 + 128 + 4) + Tkv * N2 * (2 * (256 + 128) + 4)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0.record()
+        step()
+        e1.record()
+        torch.cuda.synchronize()
+        per.append(e0.elapsed_time(e1))
+    ms = statistics.mean(per)
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt[0])
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    if rank != 0:
+        return None
+    pk, src = peaks()
+    hbm = pk.get("hbm_gbs", 6800.0)
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": "quantise step (bf16 Q rows -> e4m3 + descale, K/V append into pages) "
+                  "HBM throughput",
+        "value": world * achieved, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 -> fp8_e4m3",
+        "data": "synthetic (seeded normal)",
+        "config": {"workload": args.workload, "op": "quantize", "q_rows": T * N1,
+                   "kv_rows": Tkv * N2, "page_size": ps, "k_scale": "per_token_head",
+                   "v_scale": "per_head", "bytes_per_step": nbytes,
+                   "l2": "flushed (512 MiB write) before every step, outside the events"},
+        "ms_per_call": {"mean": ms, "median": statistics.median(per), "min": min(per)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "peak_source": f"{src}: copy bandwidth", "kernel": "quantize_rows + append_kv"},
+        "gpu_launches": 2 * args.steps,
+    }
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    if args.impl == "reference":
+    if args.impl == "reference" and args.op == "quantize":
+        line = {"impl": "reference", "unavailable": "the reference arm times the attention oracle only"}
+        if rank != 0:
+            line = None
+    elif args.impl == "reference":
         line = run_reference(args, rank)
+    elif args.op == "quantize":
+        line = run_quantize(args, rank, world)
     else:
         line = run_ours(args, rank, world)
     if line is not None:

@@ -1,7 +1,8 @@
 """Block-sparse FP8 attention prefill over a paged KV cache on GB300 (sm_103a).
 
 A thin ctypes binding over the C ABI in include/bsa_fp8.h: it marshals PyTorch CUDA tensors
-(device pointers) and the current stream into ``bsa_fp8_prefill`` / ``bsa_fp8_compact_tiles``.
+(device pointers) and the current stream into ``bsa_fp8_prefill`` / ``bsa_fp8_compact_tiles``
+and the quantise step ``bsa_fp8_quantize_rows`` / ``bsa_fp8_append_kv``.
 Every step of the computation runs in the library's CUDA kernels; there is no CPU path.
 The library must have been built (``block_sparse_fp8_gb300._build.build()``); importing the
 binding on a machine without it raises immediately.
@@ -14,7 +15,8 @@ import os
 
 from . import _build
 
-__all__ = ["Dims", "prefill", "compact_tiles", "workspace_size", "status_string", "lib",
+__all__ = ["Dims", "AppendDims", "prefill", "compact_tiles", "quantize_rows", "append_kv",
+           "workspace_size", "status_string", "lib",
            "SCALE_PER_TENSOR", "SCALE_PER_TOKEN_HEAD", "SCALE_PER_HEAD", "BsaError",
            "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_BAD_SEQLEN", "DEV_TIMEOUT"]
 
@@ -28,7 +30,8 @@ DEV_BAD_SEQLEN = 4
 DEV_TIMEOUT = 8
 
 EXPORTED = ("bsa_fp8_prefill", "bsa_fp8_prefill_workspace_size", "bsa_fp8_compact_tiles",
-            "bsa_fp8_prefill_noalloc", "bsa_status_string")
+            "bsa_fp8_prefill_noalloc", "bsa_fp8_quantize_rows", "bsa_fp8_append_kv",
+            "bsa_status_string")
 
 
 class BsaError(RuntimeError):
@@ -41,6 +44,12 @@ class Dims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "B", "N1", "N2", "D", "page_size", "max_q_len", "max_kv_len", "num_pages",
         "max_pages_per_seq", "total_q", "k_scale_kind", "v_scale_kind", "causal")]
+
+
+class AppendDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "B", "N2", "D", "page_size", "num_pages", "max_pages_per_seq", "total_new",
+        "k_scale_kind", "v_scale_kind")]
 
 
 _lib = None
@@ -65,6 +74,10 @@ def lib():
                                                                                   vp, vp, vp]
         L.bsa_fp8_compact_tiles.restype = i32
         L.bsa_fp8_compact_tiles.argtypes = [ctypes.POINTER(Dims)] + [vp] * 9
+        L.bsa_fp8_quantize_rows.restype = i32
+        L.bsa_fp8_quantize_rows.argtypes = [vp, ctypes.c_longlong, vp, vp, vp]
+        L.bsa_fp8_append_kv.restype = i32
+        L.bsa_fp8_append_kv.argtypes = [ctypes.POINTER(AppendDims)] + [vp] * 12
         L.bsa_status_string.restype = ctypes.c_char_p
         L.bsa_status_string.argtypes = [i32]
         _lib = L
@@ -161,3 +174,40 @@ def compact_tiles(cu_seqlens_q, seqused_kv, dims: Dims, block_mask=None, sparse_
     if st != 0:
         raise BsaError(st, "bsa_fp8_compact_tiles")
     return lists, counts
+
+
+def quantize_rows(x, codes=None, descale=None, stream=None):
+    """bf16 tensor [..., 128] -> (e4m3 codes uint8 [..., 128], fp32 descale [...]): per row
+    descale = amax / 448 (1 for a zero row), code = e4m3(x / descale)."""
+    import torch
+
+    if x.dtype != torch.bfloat16 or x.shape[-1] != 128 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 tensor [..., 128]")
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if descale is None:
+        descale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    st = lib().bsa_fp8_quantize_rows(_p(x), x.numel() // 128, _p(codes), _p(descale),
+                                     _stream_handle(stream))
+    if st != 0:
+        raise BsaError(st, "bsa_fp8_quantize_rows")
+    return codes, descale
+
+
+def append_kv(k_new, v_new, cu_seqlens_new, cache_seqlens, block_table, k_pages, v_pages,
+              k_descale=None, k_scale=None, v_scale=None, k_scale_kind=SCALE_PER_TOKEN_HEAD,
+              v_scale_kind=SCALE_PER_HEAD, dev_status=None, stream=None):
+    """Writes bf16 K/V tokens [T_new, N2, 128] into the paged cache (k_pages / v_pages
+    [P, N2, page_size, 128] uint8 e4m3, k_descale [P, N2, page_size] for per-token K) at
+    positions cache_seqlens[b] + i through block_table [B, L]; in place."""
+    P, N2, ps, D = k_pages.shape
+    dims = AppendDims(B=cu_seqlens_new.numel() - 1, N2=N2, D=D, page_size=ps, num_pages=P,
+                      max_pages_per_seq=block_table.shape[1], total_new=k_new.shape[0],
+                      k_scale_kind=k_scale_kind, v_scale_kind=v_scale_kind)
+    st = lib().bsa_fp8_append_kv(ctypes.byref(dims), _p(k_new), _p(v_new), _p(cu_seqlens_new),
+                                 _p(cache_seqlens), _p(block_table), _p(k_scale), _p(v_scale),
+                                 _p(k_pages), _p(v_pages), _p(k_descale), _p(dev_status),
+                                 _stream_handle(stream))
+    if st != 0:
+        raise BsaError(st, "bsa_fp8_append_kv")
+    return k_pages, v_pages, k_descale

@@ -5,6 +5,8 @@
 //     KV tiles (warp ballot stream compaction; hpc-ops Block-Sparse FP8 Attention, section
 //     活跃 tile 列表).  The attention kernel runs the same device function on its own tasks.
 //   * attn::bsa_attention_kernel (bsa_attention.cuh) -- the persistent prefill kernel.
+//   * quant::quantize_rows_kernel / quant::append_kv_kernel (bsa_quant.cuh) -- the quantise
+//     step that produces the prefill's e4m3 inputs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -19,6 +21,7 @@
 #include "bsa_attention.cuh"
 #include "bsa_common.cuh"
 #include "bsa_fp8.h"
+#include "bsa_quant.cuh"
 #include "ptx_sm103.cuh"
 
 namespace bsa {
@@ -301,6 +304,94 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
     return BSA_ERR_CUDA;
   attn::bsa_attention_kernel<<<(unsigned)grid, attn::NTHREADS, smem, (cudaStream_t)stream>>>(
       p, tq, tk, tv);
+  return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------------------
+// quantise step
+// ------------------------------------------------------------------------------------------
+
+namespace {
+
+// grid for `rows` half-warp rows (two per half-warp step): enough blocks to cover them, at
+// most as many as are resident at once
+template <typename Kernel>
+bsa_status_t quant_grid(Kernel kernel, long long rows, unsigned *grid) {
+  int num_sms = 0, per_sm = 0;
+  const bsa_status_t st = check_device(0, &num_sms);
+  if (st != BSA_OK) return st;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, quant::THREADS, 0) !=
+      cudaSuccess)
+    return BSA_ERR_CUDA;
+  const long long per_block = 2 * (quant::THREADS / 16);
+  const long long need = (rows + per_block - 1) / per_block;
+  *grid = (unsigned)std::max<long long>(
+      1, std::min<long long>(need, (long long)std::max(per_sm, 1) * num_sms));
+  return BSA_OK;
+}
+
+}  // namespace
+
+extern "C" bsa_status_t bsa_fp8_quantize_rows(const void *x_bf16, long long rows,
+                                              void *codes_e4m3, float *descale, void *stream) {
+  if (rows < 0) return BSA_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return BSA_OK;
+  if (!x_bf16 || !codes_e4m3 || !descale || !aligned16(x_bf16) || !aligned16(codes_e4m3))
+    return BSA_ERR_INVALID_ARGUMENT;
+  unsigned grid = 0;
+  const bsa_status_t st = quant_grid(quant::quantize_rows_kernel, rows, &grid);
+  if (st != BSA_OK) return st;
+  quant::quantize_rows_kernel<<<grid, quant::THREADS, 0, (cudaStream_t)stream>>>(
+      static_cast<const uint4 *>(x_bf16), rows, static_cast<uint2 *>(codes_e4m3), descale);
+  return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+extern "C" bsa_status_t bsa_fp8_append_kv(const bsa_fp8_append_dims_t *d, const void *k_new_bf16,
+                                          const void *v_new_bf16, const int *cu_seqlens_new,
+                                          const int *cache_seqlens, const int *block_table,
+                                          const float *k_scale, const float *v_scale,
+                                          void *k_pages, void *v_pages, float *k_descale,
+                                          int *dev_status, void *stream) {
+  if (!d || d->D != HEAD_DIM || (d->page_size != 32 && d->page_size != 64) || d->B < 0 ||
+      d->N2 < 1 || d->num_pages < 0 || d->max_pages_per_seq < 0 || d->total_new < 0)
+    return BSA_ERR_INVALID_ARGUMENT;
+  if (d->k_scale_kind != BSA_SCALE_PER_TOKEN_HEAD && d->k_scale_kind != BSA_SCALE_PER_TENSOR)
+    return BSA_ERR_INVALID_ARGUMENT;
+  if (d->v_scale_kind != BSA_SCALE_PER_HEAD && d->v_scale_kind != BSA_SCALE_PER_TENSOR)
+    return BSA_ERR_INVALID_ARGUMENT;
+  const long long rows = (long long)d->total_new * d->N2;
+  if (rows == 0 || d->B == 0) return BSA_OK;
+  const bool k_tok = d->k_scale_kind == BSA_SCALE_PER_TOKEN_HEAD;
+  if (!k_new_bf16 || !v_new_bf16 || !cu_seqlens_new || !cache_seqlens || !block_table ||
+      !v_scale || !k_pages || !v_pages || (k_tok ? !k_descale : !k_scale))
+    return BSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(k_new_bf16) || !aligned16(v_new_bf16) || !aligned16(k_pages) ||
+      !aligned16(v_pages))
+    return BSA_ERR_INVALID_ARGUMENT;
+  unsigned grid = 0;
+  const bsa_status_t st = quant_grid(quant::append_kv_kernel, rows, &grid);
+  if (st != BSA_OK) return st;
+  quant::AppendParams p;
+  p.k_new = static_cast<const uint4 *>(k_new_bf16);
+  p.v_new = static_cast<const uint4 *>(v_new_bf16);
+  p.cu_new = cu_seqlens_new;
+  p.cache_len = cache_seqlens;
+  p.block_table = block_table;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.k_pages = static_cast<uint2 *>(k_pages);
+  p.v_pages = static_cast<uint2 *>(v_pages);
+  p.k_descale = k_descale;
+  p.dev_status = dev_status;
+  p.B = d->B;
+  p.N2 = d->N2;
+  p.ps = d->page_size;
+  p.num_pages = d->num_pages;
+  p.L = d->max_pages_per_seq;
+  p.total_new = d->total_new;
+  p.k_per_token = k_tok ? 1 : 0;
+  p.v_per_head = d->v_scale_kind == BSA_SCALE_PER_HEAD ? 1 : 0;
+  quant::append_kv_kernel<<<grid, quant::THREADS, 0, (cudaStream_t)stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 

@@ -1,0 +1,175 @@
+// The quantise step before the attention call: bf16 rows of 128 values -> e4m3 codes and an
+// fp32 descale per row (FlashMLA page, section 量化 / 解量化的源码实现: scale = amax / 448,
+// stored value e4m3(x / scale)), and the K/V append into the paged cache.
+//
+// HBM-bound.  A half-warp owns one 256-byte row: each lane loads 16 bytes (8 values), the row
+// maximum combines in four shuffles, and each lane stores its 8 codes (8 bytes), so a warp
+// reads 512 and writes 256 contiguous bytes per step.  The quotient is the correctly rounded
+// fp32 x / scale (the code decision is taken in that precision on every side) and the
+// conversion rounds to nearest even with saturation.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "bsa_common.cuh"
+
+namespace bsa {
+namespace quant {
+
+constexpr int THREADS = 256;  // 16 rows per block step
+
+__device__ __forceinline__ void report_status(int *dev_status, int bits) {
+  if (dev_status) atomicOr(dev_status, bits);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &w, float (&v)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(u[i] << 16);
+    v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+  }
+}
+
+// Largest |v| of the 128 values of the half-warp's row.
+__device__ __forceinline__ float row_amax(const float (&v)[8]) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  return a;
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+
+// 8 codes of v / scale, the first value in the lowest byte.  The quotients are the correctly
+// rounded fp32 quotients.  For a scale in [2^-90, 2^90] they come from Markstein's correction
+// (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000 processor",
+// IBM J. Res. Dev. 34(1), 1990): with r the correctly rounded reciprocal of the scale,
+// q0 = x*r, the remainder x - q0*scale (exact in one fma) and q = q0 + remainder*r rounded
+// once give the correctly rounded x / scale whenever no intermediate leaves the normal range,
+// which that scale range guarantees for every quotient that can round to a nonzero e4m3 code;
+// three operations per value instead of a full division.  Other scales divide directly.
+__device__ __forceinline__ uint2 codes8(const float (&v)[8], float scale) {
+  float q[8];
+  if (scale >= 0x1p-90f && scale <= 0x1p90f) {
+    const float r = __frcp_rn(scale);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float q0 = v[i] * r;
+      q[i] = fmaf(fmaf(-q0, scale, v[i]), r, q0);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(v[i], scale);
+  }
+  return make_uint2(e4m3x4(q[0], q[1], q[2], q[3]), e4m3x4(q[4], q[5], q[6], q[7]));
+}
+
+__device__ __forceinline__ float descale_of(float amax) {
+  return amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+}
+
+__global__ void __launch_bounds__(THREADS) quantize_rows_kernel(const uint4 *__restrict__ x,
+                                                                long long rows,
+                                                                uint2 *__restrict__ codes,
+                                                                float *__restrict__ descale) {
+  const int lane = threadIdx.x & 15;
+  const long long step = (long long)gridDim.x * (THREADS / 16);
+  // every lane runs the same number of iterations (the shuffles need the whole warp); each
+  // iteration takes two rows, both loads in flight before either is used
+  const long long first = (long long)blockIdx.x * (THREADS / 16) + (threadIdx.x >> 4);
+  const long long iters = (rows + 2 * step - 1) / (2 * step);
+  for (long long it = 0; it < iters; ++it) {
+    const long long r0 = first + 2 * it * step, r1 = r0 + step;
+    const bool live0 = r0 < rows, live1 = r1 < rows;
+    const uint4 w0 = live0 ? x[r0 * 16 + lane] : make_uint4(0, 0, 0, 0);
+    const uint4 w1 = live1 ? x[r1 * 16 + lane] : make_uint4(0, 0, 0, 0);
+    float v[8];
+    unpack8(w0, v);
+    const float d0 = descale_of(row_amax(v));
+    if (live0) {
+      codes[r0 * 16 + lane] = codes8(v, d0);
+      if (lane == 0) descale[r0] = d0;
+    }
+    unpack8(w1, v);
+    const float d1 = descale_of(row_amax(v));
+    if (live1) {
+      codes[r1 * 16 + lane] = codes8(v, d1);
+      if (lane == 0) descale[r1] = d1;
+    }
+  }
+}
+
+struct AppendParams {
+  const uint4 *k_new, *v_new;
+  const int *cu_new, *cache_len, *block_table;
+  const float *k_scale, *v_scale;
+  uint2 *k_pages, *v_pages;
+  float *k_descale;
+  int *dev_status;
+  int B, N2, ps, num_pages, L, total_new;
+  int k_per_token, v_per_head;
+};
+
+__global__ void __launch_bounds__(THREADS) append_kv_kernel(const AppendParams p) {
+  const int lane = threadIdx.x & 15;
+  const long long rows = (long long)p.total_new * p.N2;
+  const long long step = (long long)gridDim.x * (THREADS / 16);
+  const long long first = (long long)blockIdx.x * (THREADS / 16) + (threadIdx.x >> 4);
+  const long long iters = (rows + step - 1) / step;
+  for (long long it = 0; it < iters; ++it) {
+    const long long r = first + it * step;
+    bool live = r < rows;
+    long long dst = 0;
+    int g = 0;
+    if (live) {
+      const int tok = (int)(r / p.N2);
+      g = (int)(r % p.N2);
+      // sequence of the token: the last b with cu_new[b] <= tok
+      int lo = 0, hi = p.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.cu_new[mid] <= tok) lo = mid; else hi = mid - 1;
+      }
+      const long long pos = (long long)p.cache_len[lo] + (tok - p.cu_new[lo]);
+      const long long lp = pos / p.ps;
+      const int pg = (pos >= 0 && lp < p.L) ? p.block_table[(size_t)lo * p.L + lp] : -1;
+      if (pg < 0 || pg >= p.num_pages) {
+        if (lane == 0) report_status(p.dev_status, BSA_DEV_BAD_PAGE);
+        live = false;
+      } else {
+        dst = ((long long)pg * p.N2 + g) * p.ps + pos % p.ps;
+      }
+    }
+    // K and V rows both in flight before either is used
+    const uint4 wk = live ? p.k_new[r * 16 + lane] : make_uint4(0, 0, 0, 0);
+    const uint4 wv = live ? p.v_new[r * 16 + lane] : make_uint4(0, 0, 0, 0);
+    float v[8];
+    unpack8(wk, v);
+    // the shuffles of row_amax run on every lane, live or not
+    const float amax = row_amax(v);
+    if (live) {
+      const float d = p.k_per_token ? descale_of(amax) : p.k_scale[0];
+      p.k_pages[dst * 16 + lane] = codes8(v, d);
+      if (p.k_per_token && lane == 0) p.k_descale[dst] = d;
+      unpack8(wv, v);
+      p.v_pages[dst * 16 + lane] = codes8(v, p.v_per_head ? p.v_scale[g] : p.v_scale[0]);
+    }
+  }
+}
+
+}  // namespace quant
+}  // namespace bsa

@@ -180,6 +180,53 @@ bsa_status_t bsa_fp8_prefill_noalloc(const bsa_fp8_dims_t *dims, const void *q,
                                      float p_scale, void *out_bf16, float *lse_f32,
                                      int *dev_status, void *stream);
 
+/* ------------------------------------------------------------------------------------------
+ * The quantise step before the attention call: bf16 inputs into the e4m3 + descale format
+ * above.  Rule (FlashMLA page, section 量化 / 解量化的源码实现, applied per 128-element row
+ * at the granularities the attention pages give): descale = amax / 448 (largest finite
+ * e4m3), computed in fp32, or 1 for an all-zero row; code = e4m3(x / descale) with an fp32
+ * division, rounded to nearest even and saturated to +-448.  Inputs must be finite.
+ * ------------------------------------------------------------------------------------------ */
+
+/* Quantises `rows` rows of 128 bf16 values (x_bf16 [rows, 128], e.g. Q [T, N1, 128] as
+ * rows = T * N1) into codes_e4m3 [rows, 128] and one fp32 descale per row (descale [rows],
+ * e.g. q_descale [T, N1]).  x_bf16 and codes_e4m3 must be 16-byte aligned.  rows = 0 is a
+ * no-op.  Returns BSA_ERR_INVALID_ARGUMENT for null pointers, misalignment or rows < 0. */
+bsa_status_t bsa_fp8_quantize_rows(const void *x_bf16, long long rows, void *codes_e4m3,
+                                   float *descale, void *stream);
+
+typedef struct {
+  int B;                 /* sequences */
+  int N2;                /* KV heads */
+  int D;                 /* head dim, must be 128 */
+  int page_size;         /* 32 or 64 */
+  int num_pages;         /* P */
+  int max_pages_per_seq; /* L, columns of block_table */
+  int total_new;         /* T_new = cu_seqlens_new[B], rows of k_new / v_new */
+  bsa_scale_kind_t k_scale_kind; /* BSA_SCALE_PER_TOKEN_HEAD (computed) or BSA_SCALE_PER_TENSOR */
+  bsa_scale_kind_t v_scale_kind; /* BSA_SCALE_PER_HEAD or BSA_SCALE_PER_TENSOR (given) */
+} bsa_fp8_append_dims_t;
+
+/* Appends new tokens to the paged K/V cache.  Token i of sequence b is row cu_seqlens_new[b]
+ * + i of k_new_bf16 / v_new_bf16 [total_new, N2, 128] and lands at logical position
+ * pos = cache_seqlens[b] + i: page block_table[b, pos / page_size], slot pos % page_size of
+ * k_pages / v_pages [P, N2, page_size, 128] e4m3.
+ *   K, BSA_SCALE_PER_TOKEN_HEAD: each (token, head) row is quantised by the rule above and
+ *      its descale written to k_descale [P, N2, page_size] (k_scale unused, may be NULL).
+ *   K, BSA_SCALE_PER_TENSOR: codes = e4m3(x / k_scale[0]) (k_descale unused, may be NULL).
+ *   V: codes = e4m3(x / v_scale[head]) for BSA_SCALE_PER_HEAD (v_scale [N2]) or
+ *      e4m3(x / v_scale[0]) for BSA_SCALE_PER_TENSOR; the caller chooses the V scale.
+ * cu_seqlens_new [B + 1], cache_seqlens [B], block_table [B, L] are device int32.  A token
+ * whose page is missing (position beyond L pages, or an entry outside [0, P)) is skipped and
+ * BSA_DEV_BAD_PAGE is OR-ed into *dev_status (if given).  Every other slot of the cache is
+ * left untouched.  k_new / v_new must be 16-byte aligned.  Counterpart of nothing in the
+ * attention pages' interface: it writes their inputs. */
+bsa_status_t bsa_fp8_append_kv(const bsa_fp8_append_dims_t *dims, const void *k_new_bf16,
+                               const void *v_new_bf16, const int *cu_seqlens_new,
+                               const int *cache_seqlens, const int *block_table,
+                               const float *k_scale, const float *v_scale, void *k_pages,
+                               void *v_pages, float *k_descale, int *dev_status, void *stream);
+
 /* Static text for a status code. */
 const char *bsa_status_string(bsa_status_t status);
 
