@@ -15,7 +15,7 @@ import os
 
 from . import _build
 
-__all__ = ["Dims", "AppendDims", "prefill", "compact_tiles", "quantize_rows", "append_kv",
+__all__ = ["Dims", "AppendDims", "Q_TND", "Q_NTD", "KV_HND", "KV_NHD", "prefill", "compact_tiles", "quantize_rows", "append_kv",
            "workspace_size", "status_string", "lib",
            "SCALE_PER_TENSOR", "SCALE_PER_TOKEN_HEAD", "SCALE_PER_HEAD", "BsaError",
            "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_BAD_SEQLEN", "DEV_TIMEOUT"]
@@ -43,13 +43,18 @@ class BsaError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "B", "N1", "N2", "D", "page_size", "max_q_len", "max_kv_len", "num_pages",
-        "max_pages_per_seq", "total_q", "k_scale_kind", "v_scale_kind", "causal")]
+        "max_pages_per_seq", "total_q", "k_scale_kind", "v_scale_kind", "causal", "q_layout",
+        "kv_layout")]
+
+
+Q_TND, Q_NTD = 0, 1
+KV_HND, KV_NHD = 0, 1
 
 
 class AppendDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "B", "N2", "D", "page_size", "num_pages", "max_pages_per_seq", "total_new",
-        "k_scale_kind", "v_scale_kind")]
+        "k_scale_kind", "v_scale_kind", "kv_layout")]
 
 
 _lib = None
@@ -100,14 +105,20 @@ def _stream_handle(stream):
 
 
 def make_dims(q, k_pages, block_table, cu_seqlens_q, max_q_len, max_kv_len, k_scale_kind,
-              v_scale_kind, causal=True) -> Dims:
-    T, N1, D = q.shape
-    P, N2, ps, D2 = k_pages.shape
+              v_scale_kind, causal=True, q_layout=Q_TND, kv_layout=KV_HND) -> Dims:
+    if q_layout == Q_NTD:
+        N1, T, D = q.shape
+    else:
+        T, N1, D = q.shape
+    if kv_layout == KV_NHD:
+        P, ps, N2, D2 = k_pages.shape
+    else:
+        P, N2, ps, D2 = k_pages.shape
     return Dims(B=cu_seqlens_q.shape[0] - 1, N1=N1, N2=N2, D=D, page_size=ps,
                 max_q_len=int(max_q_len), max_kv_len=int(max_kv_len), num_pages=P,
                 max_pages_per_seq=block_table.shape[1], total_q=T,
                 k_scale_kind=int(k_scale_kind), v_scale_kind=int(v_scale_kind),
-                causal=int(bool(causal)))
+                causal=int(bool(causal)), q_layout=int(q_layout), kv_layout=int(kv_layout))
 
 
 def workspace_size(dims: Dims) -> int:
@@ -119,10 +130,12 @@ def prefill(q, k_pages, v_pages, q_descale, k_descale, v_descale, cu_seqlens_q, 
             sparse_seq_len=None, softmax_scale: float | None = None, p_scale: float = 256.0,
             causal: bool = True, out=None, lse=None, return_lse: bool = True, dev_status=None,
             workspace=None, stream=None, k_scale_kind: int | None = None,
-            v_scale_kind: int | None = None):
+            v_scale_kind: int | None = None, q_layout: int = Q_TND, kv_layout: int = KV_HND):
     """Block-sparse FP8 prefill.  Tensors are CUDA tensors in the C ABI's layouts:
-    q uint8/float8_e4m3fn [T, N1, 128]; k_pages, v_pages [P, N2, page, 128]; q_descale f32
-    [T, N1]; k_descale f32 [1] or [P, N2, page]; v_descale f32 [1] or [N2]; cu_seqlens_q i32
+    q uint8/float8_e4m3fn [T, N1, 128] (q_layout Q_TND) or [N1, T, 128] (Q_NTD, with q_descale
+    [N1, T]); k_pages, v_pages [P, N2, page, 128] (KV_HND) or [P, page, N2, 128] (KV_NHD);
+    q_descale f32 [T, N1]; k_descale f32 [1] or [P, N2, page]; v_descale f32 [1] or [N2];
+    cu_seqlens_q i32
     [B+1]; seqused_kv i32 [B] or None; block_table i32 [B, L]; block_mask u8 [B, N1, Qb, Kb]
     or sparse_indices i32 [B, N1, Qb, Kb] + sparse_seq_len i32 [B, N1, Qb].
     max_q_len / max_kv_len are host integers (upper bounds of the per-sequence lengths).
@@ -131,13 +144,14 @@ def prefill(q, k_pages, v_pages, q_descale, k_descale, v_descale, cu_seqlens_q, 
     Returns (out bf16 [T, N1, 128], lse f32 [N1, T] or None)."""
     import torch
 
+    n2 = k_pages.shape[2] if kv_layout == KV_NHD else k_pages.shape[1]
     k_kind = k_scale_kind if k_scale_kind is not None else (
         SCALE_PER_TOKEN_HEAD if k_descale.dim() == 3 else SCALE_PER_TENSOR)
     v_kind = v_scale_kind if v_scale_kind is not None else (
-        SCALE_PER_HEAD if v_descale.numel() == k_pages.shape[1] else SCALE_PER_TENSOR)
+        SCALE_PER_HEAD if v_descale.numel() == n2 else SCALE_PER_TENSOR)
     dims = make_dims(q, k_pages, block_table, cu_seqlens_q, max_q_len, max_kv_len, k_kind,
-                     v_kind, causal)
-    T, N1, D = q.shape
+                     v_kind, causal, q_layout, kv_layout)
+    T, N1, D = dims.total_q, dims.N1, dims.D
     if out is None:
         out = torch.empty((T, N1, D), dtype=torch.bfloat16, device=q.device)
     if lse is None and return_lse:
@@ -196,14 +210,19 @@ def quantize_rows(x, codes=None, descale=None, stream=None):
 
 def append_kv(k_new, v_new, cu_seqlens_new, cache_seqlens, block_table, k_pages, v_pages,
               k_descale=None, k_scale=None, v_scale=None, k_scale_kind=SCALE_PER_TOKEN_HEAD,
-              v_scale_kind=SCALE_PER_HEAD, dev_status=None, stream=None):
+              v_scale_kind=SCALE_PER_HEAD, dev_status=None, stream=None, kv_layout=KV_HND):
     """Writes bf16 K/V tokens [T_new, N2, 128] into the paged cache (k_pages / v_pages
-    [P, N2, page_size, 128] uint8 e4m3, k_descale [P, N2, page_size] for per-token K) at
-    positions cache_seqlens[b] + i through block_table [B, L]; in place."""
-    P, N2, ps, D = k_pages.shape
+    [P, N2, page_size, 128] (KV_HND) or [P, page_size, N2, 128] (KV_NHD) uint8 e4m3,
+    k_descale [P, N2, page_size] for per-token K) at positions cache_seqlens[b] + i through
+    block_table [B, L]; in place."""
+    if kv_layout == KV_NHD:
+        P, ps, N2, D = k_pages.shape
+    else:
+        P, N2, ps, D = k_pages.shape
     dims = AppendDims(B=cu_seqlens_new.numel() - 1, N2=N2, D=D, page_size=ps, num_pages=P,
                       max_pages_per_seq=block_table.shape[1], total_new=k_new.shape[0],
-                      k_scale_kind=k_scale_kind, v_scale_kind=v_scale_kind)
+                      k_scale_kind=k_scale_kind, v_scale_kind=v_scale_kind,
+                      kv_layout=int(kv_layout))
     st = lib().bsa_fp8_append_kv(ctypes.byref(dims), _p(k_new), _p(v_new), _p(cu_seqlens_new),
                                  _p(cache_seqlens), _p(block_table), _p(k_scale), _p(v_scale),
                                  _p(k_pages), _p(v_pages), _p(k_descale), _p(dev_status),

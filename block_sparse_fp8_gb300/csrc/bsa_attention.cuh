@@ -208,7 +208,8 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
       if (qk >= 1 && !wait_bar(p, s, &s.q_empty, (qk - 1) & 1)) ok = false;
       if (ok) {
         ptx::mbar_arrive_expect_tx(&s.q_full, TILE * HEAD_DIM);
-        ptx::tma_load_3d(s.q, tmap_q, &s.q_full, 0, h, geo.q0 + qt * TILE);
+        const int tok0 = geo.q0 + qt * TILE;  // the Q box is 128 tokens of head h either way
+        ptx::tma_load_3d(s.q, tmap_q, &s.q_full, 0, p.q_ntd ? tok0 : h, p.q_ntd ? h : tok0);
       }
       ++qk;
       int prev[4] = {0, 0, 0, 0};
@@ -227,8 +228,8 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             if (i < npg)
-              ptx::tma_load_4d(s.k[ks] + i * p.ps * HEAD_DIM, tmap_k, &s.k_full[ks], 0, 0, g_kv,
-                               pgs[i]);
+              ptx::tma_load_4d(s.k[ks] + i * p.ps * HEAD_DIM, tmap_k, &s.k_full[ks], 0,
+                               p.kv_nhd ? g_kv : 0, p.kv_nhd ? 0 : g_kv, pgs[i]);
           if (p.k_per_token) {
             const int ds = gk % KDSTAGES;
             if (gk >= KDSTAGES && !wait_bar(p, s, &s.kd_empty[ds], ((gk / KDSTAGES) - 1) & 1)) {
@@ -257,8 +258,8 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             if (i < npg)
-              ptx::tma_load_4d(s.v[vs] + i * p.ps * HEAD_DIM, tmap_v, &s.v_full[vs], 0, 0, g_kv,
-                               prev[i]);
+              ptx::tma_load_4d(s.v[vs] + i * p.ps * HEAD_DIM, tmap_v, &s.v_full[vs], 0,
+                               p.kv_nhd ? g_kv : 0, p.kv_nhd ? 0 : g_kv, prev[i]);
         }
         if (t < n) {
 #pragma unroll
@@ -408,7 +409,9 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
       const int qt = ti.qt, h = ti.h, q_len = ti.q_len;
       const int tok = ti.q0 + qt * TILE + r;
       const float qd =
-          r < min(TILE, q_len - qt * TILE) ? p.q_descale[(size_t)tok * p.N1 + h] : 0.f;
+          r < min(TILE, q_len - qt * TILE)
+              ? p.q_descale[(size_t)tok * p.qd_tok + (size_t)h * p.qd_head]
+              : 0.f;
       row_scale = qd * p.scale_log2 * (p.k_per_token ? 1.f : p.k_descale[0]);
       causal_lim = qt * TILE + r + (ti.kv_len - q_len);
     }

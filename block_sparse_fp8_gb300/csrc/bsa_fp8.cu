@@ -85,6 +85,8 @@ static bsa_status_t validate_dims(const bsa_fp8_dims_t *d) {
   if (d->v_scale_kind != BSA_SCALE_PER_TENSOR && d->v_scale_kind != BSA_SCALE_PER_HEAD)
     return BSA_ERR_INVALID_ARGUMENT;
   if (d->causal != 0 && d->causal != 1) return BSA_ERR_INVALID_ARGUMENT;
+  if (d->q_layout != BSA_Q_TND && d->q_layout != BSA_Q_NTD) return BSA_ERR_INVALID_ARGUMENT;
+  if (d->kv_layout != BSA_KV_HND && d->kv_layout != BSA_KV_NHD) return BSA_ERR_INVALID_ARGUMENT;
   if (cdiv(d->max_kv_len, TILE) > KB_MAX) return BSA_ERR_UNSUPPORTED;
   if ((long long)d->B * d->N1 * cdiv(d->max_q_len, TILE) > 0x7fffffffLL)
     return BSA_ERR_UNSUPPORTED;
@@ -164,6 +166,10 @@ static Params make_params(const bsa_fp8_dims_t *d) {
   p.k_per_token = d->k_scale_kind == BSA_SCALE_PER_TOKEN_HEAD;
   p.v_per_head = d->v_scale_kind == BSA_SCALE_PER_HEAD;
   p.causal = d->causal;
+  p.q_ntd = d->q_layout == BSA_Q_NTD;
+  p.kv_nhd = d->kv_layout == BSA_KV_NHD;
+  p.qd_tok = p.q_ntd ? 1 : d->N1;
+  p.qd_head = p.q_ntd ? d->total_q : 1;
   return p;
 }
 
@@ -283,18 +289,32 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
   // the clamped polynomial exp2 is only used where its input range is safe
   p.poly_exp = (p.log2_pscale <= 64.f && p.log2_pscale >= -32.f) ? 1 : 0;
 
+  // Tensor maps, innermost dimension first.  Either layout puts one 128-token Q box of a head,
+  // or one page of a KV head, into shared memory as consecutive 128-byte rows.
   CUtensorMap tq, tk, tv;
-  {
+  if (!p.q_ntd) {  // [T, N1, 128]: dims (d, head, token), box (128, 1, 128)
     cuuint64_t gd[3] = {HEAD_DIM, (cuuint64_t)p.N1, (cuuint64_t)p.T};
     cuuint64_t gs[2] = {HEAD_DIM, (cuuint64_t)p.N1 * HEAD_DIM};
     cuuint32_t box[3] = {HEAD_DIM, 1, TILE};
     if (!encode_map(&tq, q, 3, gd, gs, box)) return BSA_ERR_CUDA;
+  } else {         // [N1, T, 128]: dims (d, token, head), box (128, 128, 1)
+    cuuint64_t gd[3] = {HEAD_DIM, (cuuint64_t)p.T, (cuuint64_t)p.N1};
+    cuuint64_t gs[2] = {HEAD_DIM, (cuuint64_t)p.T * HEAD_DIM};
+    cuuint32_t box[3] = {HEAD_DIM, TILE, 1};
+    if (!encode_map(&tq, q, 3, gd, gs, box)) return BSA_ERR_CUDA;
   }
-  {
+  if (!p.kv_nhd) {  // [P, N2, ps, 128]: dims (d, slot, head, page), box (128, ps, 1, 1)
     cuuint64_t gd[4] = {HEAD_DIM, (cuuint64_t)p.ps, (cuuint64_t)p.N2, (cuuint64_t)p.num_pages};
     cuuint64_t gs[3] = {HEAD_DIM, (cuuint64_t)p.ps * HEAD_DIM,
                         (cuuint64_t)p.N2 * p.ps * HEAD_DIM};
     cuuint32_t box[4] = {HEAD_DIM, (cuuint32_t)p.ps, 1, 1};
+    if (!encode_map(&tk, k_pages, 4, gd, gs, box)) return BSA_ERR_CUDA;
+    if (!encode_map(&tv, v_pages, 4, gd, gs, box)) return BSA_ERR_CUDA;
+  } else {          // [P, ps, N2, 128]: dims (d, head, slot, page), box (128, 1, ps, 1)
+    cuuint64_t gd[4] = {HEAD_DIM, (cuuint64_t)p.N2, (cuuint64_t)p.ps, (cuuint64_t)p.num_pages};
+    cuuint64_t gs[3] = {HEAD_DIM, (cuuint64_t)p.N2 * HEAD_DIM,
+                        (cuuint64_t)p.ps * p.N2 * HEAD_DIM};
+    cuuint32_t box[4] = {HEAD_DIM, 1, (cuuint32_t)p.ps, 1};
     if (!encode_map(&tk, k_pages, 4, gd, gs, box)) return BSA_ERR_CUDA;
     if (!encode_map(&tv, v_pages, 4, gd, gs, box)) return BSA_ERR_CUDA;
   }
@@ -359,6 +379,7 @@ extern "C" bsa_status_t bsa_fp8_append_kv(const bsa_fp8_append_dims_t *d, const 
     return BSA_ERR_INVALID_ARGUMENT;
   if (d->v_scale_kind != BSA_SCALE_PER_HEAD && d->v_scale_kind != BSA_SCALE_PER_TENSOR)
     return BSA_ERR_INVALID_ARGUMENT;
+  if (d->kv_layout != BSA_KV_HND && d->kv_layout != BSA_KV_NHD) return BSA_ERR_INVALID_ARGUMENT;
   const long long rows = (long long)d->total_new * d->N2;
   if (rows == 0 || d->B == 0) return BSA_OK;
   const bool k_tok = d->k_scale_kind == BSA_SCALE_PER_TOKEN_HEAD;
@@ -391,6 +412,7 @@ extern "C" bsa_status_t bsa_fp8_append_kv(const bsa_fp8_append_dims_t *d, const 
   p.total_new = d->total_new;
   p.k_per_token = k_tok ? 1 : 0;
   p.v_per_head = d->v_scale_kind == BSA_SCALE_PER_HEAD ? 1 : 0;
+  p.kv_nhd = d->kv_layout == BSA_KV_NHD ? 1 : 0;
   quant::append_kv_kernel<<<grid, quant::THREADS, 0, (cudaStream_t)stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }

@@ -121,7 +121,7 @@ struct AppendParams {
   float *k_descale;
   int *dev_status;
   int B, N2, ps, num_pages, L, total_new;
-  int k_per_token, v_per_head;
+  int k_per_token, v_per_head, kv_nhd;
 };
 
 __global__ void __launch_bounds__(THREADS) append_kv_kernel(const AppendParams p) {
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(THREADS) append_kv_kernel(const AppendParams p
   for (long long it = 0; it < iters; ++it) {
     const long long r = first + it * step;
     bool live = r < rows;
-    long long dst = 0;
+    long long dst = 0, row = 0;  // descale index and 128-byte page row of the token
     int g = 0;
     if (live) {
       const int tok = (int)(r / p.N2);
@@ -151,7 +151,9 @@ __global__ void __launch_bounds__(THREADS) append_kv_kernel(const AppendParams p
         if (lane == 0) report_status(p.dev_status, BSA_DEV_BAD_PAGE);
         live = false;
       } else {
-        dst = ((long long)pg * p.N2 + g) * p.ps + pos % p.ps;
+        const long long slot = pos % p.ps;
+        dst = ((long long)pg * p.N2 + g) * p.ps + slot;  // the K descale's index [P, N2, ps]
+        row = p.kv_nhd ? ((long long)pg * p.ps + slot) * p.N2 + g : dst;
       }
     }
     // K and V rows both in flight before either is used
@@ -163,10 +165,10 @@ __global__ void __launch_bounds__(THREADS) append_kv_kernel(const AppendParams p
     const float amax = row_amax(v);
     if (live) {
       const float d = p.k_per_token ? descale_of(amax) : p.k_scale[0];
-      p.k_pages[dst * 16 + lane] = codes8(v, d);
+      p.k_pages[row * 16 + lane] = codes8(v, d);
       if (p.k_per_token && lane == 0) p.k_descale[dst] = d;
       unpack8(wv, v);
-      p.v_pages[dst * 16 + lane] = codes8(v, p.v_per_head ? p.v_scale[g] : p.v_scale[0]);
+      p.v_pages[row * 16 + lane] = codes8(v, p.v_per_head ? p.v_scale[g] : p.v_scale[0]);
     }
   }
 }

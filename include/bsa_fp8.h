@@ -71,7 +71,12 @@ typedef enum {
 /* Problem geometry (host struct).  Layouts follow the Quant Block Sparse Attention
  * parameter table with the page size made a parameter:
  *   q            e4m3 [total_q, N1, 128]            (TND; row of token t, head h at (t*N1+h)*128)
- *   k/v pages    e4m3 [num_pages, N2, page_size, 128]
+ *                or [N1, total_q, 128] (NTD) with q_layout = BSA_Q_NTD (the table's layout_q);
+ *                q_descale follows: [total_q, N1] or [N1, total_q].  out is always TND.
+ *   k/v pages    e4m3 [num_pages, N2, page_size, 128] (HND within a page), or
+ *                [num_pages, page_size, N2, 128] (NHD, the hpc-ops tests' other cache layout)
+ *                with kv_layout = BSA_KV_NHD.  The per-token K descale stays [num_pages, N2,
+ *                page_size] in both.
  *   block_table  int32 [B, max_pages_per_seq]; logical page l of sequence b -> physical page
  * Q tile = KV tile = 128 tokens; Qb = ceil(max_q_len/128), Kb = ceil(max_kv_len/128).
  * The KV head of query head h is h / (N1/N2). */
@@ -89,7 +94,14 @@ typedef struct {
   int k_scale_kind;      /* BSA_SCALE_PER_TENSOR or BSA_SCALE_PER_TOKEN_HEAD */
   int v_scale_kind;      /* BSA_SCALE_PER_TENSOR or BSA_SCALE_PER_HEAD */
   int causal;            /* 1 = right-context causal (mask_mode 3), 0 = no causal mask (mode 0) */
+  int q_layout;          /* BSA_Q_TND (0) or BSA_Q_NTD (1) */
+  int kv_layout;         /* BSA_KV_HND (0) or BSA_KV_NHD (1) */
 } bsa_fp8_dims_t;
+
+#define BSA_Q_TND 0
+#define BSA_Q_NTD 1
+#define BSA_KV_HND 0
+#define BSA_KV_NHD 1
 
 /* Bytes of device workspace bsa_fp8_prefill needs for `dims` (currently 256: the counter
  * the persistent kernel's CTAs claim tasks from; bsa_fp8_prefill zeroes it on `stream`
@@ -205,12 +217,14 @@ typedef struct {
   int total_new;         /* T_new = cu_seqlens_new[B], rows of k_new / v_new */
   bsa_scale_kind_t k_scale_kind; /* BSA_SCALE_PER_TOKEN_HEAD (computed) or BSA_SCALE_PER_TENSOR */
   bsa_scale_kind_t v_scale_kind; /* BSA_SCALE_PER_HEAD or BSA_SCALE_PER_TENSOR (given) */
+  int kv_layout;         /* BSA_KV_HND (0): pages [P, N2, page_size, 128]; BSA_KV_NHD (1):
+                            [P, page_size, N2, 128]; k_descale is [P, N2, page_size] in both */
 } bsa_fp8_append_dims_t;
 
 /* Appends new tokens to the paged K/V cache.  Token i of sequence b is row cu_seqlens_new[b]
  * + i of k_new_bf16 / v_new_bf16 [total_new, N2, 128] and lands at logical position
  * pos = cache_seqlens[b] + i: page block_table[b, pos / page_size], slot pos % page_size of
- * k_pages / v_pages [P, N2, page_size, 128] e4m3.
+ * k_pages / v_pages (e4m3, HND or NHD pages as dims->kv_layout says).
  *   K, BSA_SCALE_PER_TOKEN_HEAD: each (token, head) row is quantised by the rule above and
  *      its descale written to k_descale [P, N2, page_size] (k_scale unused, may be NULL).
  *   K, BSA_SCALE_PER_TENSOR: codes = e4m3(x / k_scale[0]) (k_descale unused, may be NULL).

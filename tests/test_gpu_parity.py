@@ -291,3 +291,33 @@ def test_workload_parity(name):
         for _ in range(2):
             o2, l2, st = run(case, d2)
             assert st == 0 and torch.equal(out, o2) and torch.equal(lse, l2)
+
+
+@pytest.mark.parametrize("name", ["bern_ragged", "indices_empty", "noncausal"])
+def test_layouts_q_ntd_and_kv_nhd(name):
+    """Q [N1, T, 128] with q_descale [N1, T], and NHD pages [P, page, N2, 128]: the same
+    arithmetic on other addresses, so every layout combination reproduces the TND / HND
+    result bit for bit, and that result matches the oracle."""
+    import block_sparse_fp8_gb300 as bsa
+
+    case = _case(name)
+    d = to_device(case)
+    base, base_lse, st = run(case, d)
+    assert st == 0
+    ref, _, err = O.Oracle(case).all_rows(O.EXACT)
+    assert err == 0
+    check_o(base.float().cpu().numpy(), ref, EXACT_ATOL, EXACT_RTOL, f"{name} vs exact")
+    q_ntd = d["q"].permute(1, 0, 2).contiguous()
+    qd_ntd = d["q_descale"].t().contiguous()
+    k_nhd = d["k_pages"].permute(0, 2, 1, 3).contiguous()
+    v_nhd = d["v_pages"].permute(0, 2, 1, 3).contiguous()
+    for ql, kl in ((bsa.Q_NTD, bsa.KV_HND), (bsa.Q_TND, bsa.KV_NHD), (bsa.Q_NTD, bsa.KV_NHD)):
+        dd = dict(d)
+        if ql == bsa.Q_NTD:
+            dd["q"], dd["q_descale"] = q_ntd, qd_ntd
+        if kl == bsa.KV_NHD:
+            dd["k_pages"], dd["v_pages"] = k_nhd, v_nhd
+        out, lse, st = run(case, dd, q_layout=ql, kv_layout=kl)
+        assert st == 0
+        assert torch.equal(out, base), f"layout ({ql}, {kl}) changed O"
+        assert torch.equal(lse, base_lse), f"layout ({ql}, {kl}) changed LSE"

@@ -130,27 +130,36 @@ def _append_case(ps, k_kind, v_kind, seed=5):
                 k_scale=k_scale, v_scale=v_scale, k_kind=k_kind, v_kind=v_kind)
 
 
-def _run_append(c):
+def _run_append(c, nhd=False):
+    """Runs the append; with nhd the cache is held as NHD pages and returned as HND."""
     import block_sparse_fp8_gb300 as bsa
 
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
-    kp, vp, kd = t(c["kp"]), t(c["vp"]), t(c["kd"])
+    perm = (0, 2, 1, 3)
+    kp = t(c["kp"].transpose(perm) if nhd else c["kp"])
+    vp = t(c["vp"].transpose(perm) if nhd else c["vp"])
+    kd = t(c["kd"])
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     bsa.append_kv(bf(c["kb"]), bf(c["vb"]), t(c["cu_new"]), t(c["cache_len"]), t(c["bt"]), kp, vp,
                   k_descale=kd, k_scale=t(c["k_scale"]), v_scale=t(c["v_scale"]),
-                  k_scale_kind=c["k_kind"], v_scale_kind=c["v_kind"], dev_status=st)
+                  k_scale_kind=c["k_kind"], v_scale_kind=c["v_kind"], dev_status=st,
+                  kv_layout=bsa.KV_NHD if nhd else bsa.KV_HND)
     torch.cuda.synchronize()
-    return kp.cpu().numpy(), vp.cpu().numpy(), kd.cpu().numpy(), int(st.item())
+    kp, vp = kp.cpu().numpy(), vp.cpu().numpy()
+    if nhd:
+        kp, vp = kp.transpose(perm), vp.transpose(perm)
+    return kp, vp, kd.cpu().numpy(), int(st.item())
 
 
+@pytest.mark.parametrize("nhd", [False, True])
 @pytest.mark.parametrize("ps", [32, 64])
 @pytest.mark.parametrize("kinds", [(W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD),
                                    (W.SCALE_PER_TENSOR, W.SCALE_PER_TENSOR)])
-def test_append_kv_bit_exact(ps, kinds):
+def test_append_kv_bit_exact(ps, kinds, nhd):
     _need_gpu()
     c = _append_case(ps, *kinds)
-    kp, vp, kd, st = _run_append(c)
+    kp, vp, kd, st = _run_append(c, nhd)
     okp, ovp, okd, err = O.append_kv(c["kb"], c["vb"], c["cu_new"], c["cache_len"], c["bt"],
                                      c["kp"], c["vp"], c["kd"], c["k_kind"], c["v_kind"],
                                      c["k_scale"], c["v_scale"])
