@@ -228,10 +228,61 @@ static const uint8_t *kv_row(const oracle_dims_t *d, const uint8_t *pages, int p
 }
 
 /* ------------------------------------------------------------------------------------
+ * The P-emulating online softmax over the active tiles tiles[t_lo .. t_hi) of one row, in
+ * order: per tile the running max m, alpha = exp(m_old - m), p = exp(x - m) in fp32, l from
+ * the unrounded p, P * p_scale rounded to e4m3 for the P.V sum.  keys [na] are the row's
+ * allowed keys in ascending order and s their logits.  Returns (m, l, acc) with acc the
+ * un-normalised sum in P-scale units; m = -inf and l = 0 when nothing is visible.
+ * ------------------------------------------------------------------------------------ */
+static int pemu_slice(const oracle_dims_t *d, const oracle_inputs_t *in, int b, int g,
+                      const int *tiles, int t_lo, int t_hi, const int *keys, const double *s,
+                      int na, double *m_out, double *l_out, double *acc) {
+  int err = 0;
+  double m = -INFINITY, l = 0.0;
+  for (int k = 0; k < HEAD_DIM; ++k) acc[k] = 0.0;
+  int a = 0;
+  for (int ti = t_lo; ti < t_hi; ++ti) {
+    int t0 = tiles[ti] * TILE;
+    while (a < na && keys[a] < t0) ++a;              /* skip keys of earlier slices */
+    int a0 = a;
+    while (a < na && keys[a] < t0 + TILE) ++a;       /* keys of this tile: [a0, a) */
+    double mt = -INFINITY;
+    for (int e = a0; e < a; ++e) {
+      double x = (double)(float)s[e];                /* the logit as a 32-bit float */
+      if (x > mt) mt = x;
+    }
+    double mn = m > mt ? m : mt;
+    if (mn == -INFINITY) continue;                   /* nothing visible yet */
+    double alpha = (m == -INFINITY) ? 0.0 : exp(m - mn);
+    double psum = 0.0;
+    double tile_acc[HEAD_DIM];
+    for (int k = 0; k < HEAD_DIM; ++k) tile_acc[k] = 0.0;
+    for (int e = a0; e < a; ++e) {
+      double x = (double)(float)s[e];
+      double p = (double)(float)exp(x - mn);
+      psum += p;
+      uint8_t p8 = oracle_e4m3_encode((double)(float)(p * in->p_scale));
+      double pq = oracle_e4m3_decode(p8);
+      int j = keys[e];
+      int pg = page_of(d, in, b, j, &err);
+      if (pg < 0) continue;
+      const uint8_t *vr = kv_row(d, in->v_pages, pg, g, j % d->page_size);
+      for (int k = 0; k < HEAD_DIM; ++k) tile_acc[k] += pq * oracle_e4m3_decode(vr[k]);
+    }
+    l = alpha * l + psum;
+    for (int k = 0; k < HEAD_DIM; ++k) acc[k] = alpha * acc[k] + tile_acc[k];
+    m = mn;
+  }
+  *m_out = m;
+  *l_out = l;
+  return err;
+}
+
+/* ------------------------------------------------------------------------------------
  * One output row (token tok of sequence b, query head h).
  * ------------------------------------------------------------------------------------ */
-static int one_row(const oracle_dims_t *d, const oracle_inputs_t *in, int mode, int tok, int h,
-                   double *o, double *lse) {
+static int one_row(const oracle_dims_t *d, const oracle_inputs_t *in, int mode, int splits,
+                   int tok, int h, double *o, double *lse) {
   int err = 0;
   int b = 0;
   while (b + 1 < d->B && in->cu_seqlens_q[b + 1] <= tok) ++b;
@@ -297,40 +348,22 @@ static int one_row(const oracle_dims_t *d, const oracle_inputs_t *in, int mode, 
     for (int k = 0; k < HEAD_DIM; ++k) o[k] /= l;
     *lse = M + log(l);
   } else {
-    /* Tiled online softmax with P rounded to e4m3 at the fixed P-scale ([HPC] 固定 P-scale). */
+    /* Tiled online softmax with P rounded to e4m3 at the fixed P-scale ([HPC] 固定 P-scale),
+     * over the whole list, or over `splits` consecutive slices of it, each from m = -inf,
+     * merged by their log-sum-exp weights (the split-KV step). */
     double m = -INFINITY, l = 0.0;
     double acc[HEAD_DIM];
     for (int k = 0; k < HEAD_DIM; ++k) acc[k] = 0.0;
-    int a = 0;
-    for (int ti = 0; ti < nt; ++ti) {
-      int t0 = tiles[ti] * TILE;
-      int a0 = a;
-      while (a < na && keys[a] < t0 + TILE) ++a;     /* keys of this tile: [a0, a) */
-      double mt = -INFINITY;
-      for (int e = a0; e < a; ++e) {
-        double x = (double)(float)s[e];              /* the logit as a 32-bit float */
-        if (x > mt) mt = x;
-      }
-      double mn = m > mt ? m : mt;
-      if (mn == -INFINITY) continue;                 /* nothing visible yet */
-      double alpha = (m == -INFINITY) ? 0.0 : exp(m - mn);
-      double psum = 0.0;
-      double tile_acc[HEAD_DIM];
-      for (int k = 0; k < HEAD_DIM; ++k) tile_acc[k] = 0.0;
-      for (int e = a0; e < a; ++e) {
-        double x = (double)(float)s[e];
-        double p = (double)(float)exp(x - mn);
-        psum += p;
-        uint8_t p8 = oracle_e4m3_encode((double)(float)(p * in->p_scale));
-        double pq = oracle_e4m3_decode(p8);
-        int j = keys[e];
-        int pg = page_of(d, in, b, j, &err);
-        if (pg < 0) continue;
-        const uint8_t *vr = kv_row(d, in->v_pages, pg, g, j % d->page_size);
-        for (int k = 0; k < HEAD_DIM; ++k) tile_acc[k] += pq * oracle_e4m3_decode(vr[k]);
-      }
-      l = alpha * l + psum;
-      for (int k = 0; k < HEAD_DIM; ++k) acc[k] = alpha * acc[k] + tile_acc[k];
+    int ns = splits < 1 ? 1 : splits;
+    for (int c = 0; c < ns; ++c) {
+      double mc, lc, accc[HEAD_DIM];
+      err |= pemu_slice(d, in, b, g, tiles, (int)((long)c * nt / ns), (int)((long)(c + 1) * nt / ns),
+                        keys, s, na, &mc, &lc, accc);
+      if (lc == 0.0 || mc == -INFINITY) continue;    /* an empty slice adds nothing */
+      double mn = m > mc ? m : mc;
+      double wo = (m == -INFINITY) ? 0.0 : exp(m - mn), wc = exp(mc - mn);
+      l = wo * l + wc * lc;
+      for (int k = 0; k < HEAD_DIM; ++k) acc[k] = wo * acc[k] + wc * accc[k];
       m = mn;
     }
     if (l == 0.0 || m == -INFINITY) {
@@ -348,8 +381,9 @@ static int one_row(const oracle_dims_t *d, const oracle_inputs_t *in, int mode, 
 
 /* Rows given as (token, head) pairs; o [nrows, 128], lse [nrows].  Returns the OR of the data
  * errors met.  nthreads <= 0 means the OpenMP default. */
-int oracle_attention_rows(const oracle_dims_t *d, const oracle_inputs_t *in, int mode,
-                          const int *rows, long nrows, double *o, double *lse, int nthreads) {
+int oracle_attention_rows_split(const oracle_dims_t *d, const oracle_inputs_t *in, int mode,
+                                int splits, const int *rows, long nrows, double *o, double *lse,
+                                int nthreads) {
   if (!d || !in || d->D != HEAD_DIM || d->N2 <= 0 || d->N1 % d->N2 != 0) return ORACLE_BAD_ARG;
   if (mode == ORACLE_PEMU && !(in->p_scale > 0.0)) return ORACLE_BAD_ARG;
   int err = 0;
@@ -358,9 +392,15 @@ int oracle_attention_rows(const oracle_dims_t *d, const oracle_inputs_t *in, int
 #pragma omp parallel for schedule(dynamic, 16) reduction(| : err)
 #endif
   for (long r = 0; r < nrows; ++r)
-    err |= one_row(d, in, mode, rows[2 * r], rows[2 * r + 1], o + r * HEAD_DIM, lse + r);
+    err |= one_row(d, in, mode, splits, rows[2 * r], rows[2 * r + 1], o + r * HEAD_DIM, lse + r);
   (void)nthreads;
   return err;
+}
+
+/* The whole active list in one online softmax (splits = 1). */
+int oracle_attention_rows(const oracle_dims_t *d, const oracle_inputs_t *in, int mode,
+                          const int *rows, long nrows, double *o, double *lse, int nthreads) {
+  return oracle_attention_rows_split(d, in, mode, 1, rows, nrows, o, lse, nthreads);
 }
 
 int oracle_max_threads(void) {

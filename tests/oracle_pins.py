@@ -508,6 +508,59 @@ def pin_pemu_near_exact(lib):
     assert np.all(np.abs(l2 - l) <= 2.5e-5 + 0.005 * np.abs(l))
 
 
+def pin_split_two_tiles(lib):
+    """The P-emulating mode with the list cut into 2 slices (one tile each, each slice its own
+    online softmax, merged by log-sum-exp weights).  Row 255: slice 0 has m = 0 and p = 1;
+    slice 1 has its own max m = -0.1, so its p = 1 too and 256p = 256 is exact; the merge
+    weighs slice 1 by e^-0.1.  O = (128*256*1 + e*128*256*2) / (256 * 128 (1 + e)) =
+    (1 + 2e) / (1 + e) -- the exact answer, unlike the unsplit mode (704 / (256 (1 + e))),
+    and LSE = ln(128 (1 + e))."""
+    case = _two_tile_case()
+    e = math.exp(float(np.float32(-0.1)))
+    o, lse, _ = _oracle(case, lib).all_rows(O.PEMU, splits=2)
+    assert abs(o[255, 0, 3] - (1 + 2 * e) / (1 + e)) < 1e-9
+    assert abs(lse[0, 255] - math.log(128 * (1 + e))) < 1e-9
+    assert abs(o[127, 0, 9] - 1.0) < 1e-12 and abs(lse[0, 127] - math.log(128)) < 1e-12
+    o1, _, _ = _oracle(case, lib).all_rows(O.PEMU, splits=1)
+    assert abs(o1[255, 0, 3] - 704.0 / (256.0 * (1 + e))) < 1e-6
+
+
+def pin_split_closed_form_zero_k(lib):
+    """K = 0 with the list in 3 and 5 slices: still every visible key at weight 1/|A_i|."""
+    case = _uniform_k_case(35)
+    sets = tile_sets(case)
+    V = torch_decode(case.meta["v_codes"]) * float(case.v_descale[0])
+    G = case.N1 // case.N2
+    for splits in (3, 5):
+        o, lse, _ = _oracle(case, lib).all_rows(O.PEMU, splits=splits)
+        kv0 = 0
+        for b in range(case.B):
+            ql, kl = case.q_lens[b], case.kv_lens[b]
+            q0 = int(case.cu_seqlens_q[b])
+            for h in range(case.N1):
+                for i in range(ql):
+                    vis = [j for j in range(kl) if j <= i + kl - ql and (j // 128) in sets[b, h, i // 128]]
+                    if not vis:
+                        assert lse[h, q0 + i] == NEG_FLT_MAX and not o[q0 + i, h].any()
+                        continue
+                    _close(o[q0 + i, h], V[[kv0 + j for j in vis], h // G].mean(axis=0), 1e-12)
+                    assert abs(lse[h, q0 + i] - math.log(len(vis))) < 1e-12
+            kv0 += kl
+
+
+def pin_split_near_exact(lib):
+    """Split P-emulation stays within the exact band like the unsplit mode."""
+    case = W.make_case("pes", 42, [384], [1600], 4, 2, 64, W.SCALE_PER_TOKEN_HEAD,
+                       W.SCALE_PER_HEAD, "bernoulli", keep=0.6)
+    a = _oracle(case, lib)
+    o, l, _ = a.all_rows(O.EXACT)
+    for splits in (2, 4):
+        o2, l2, _ = a.all_rows(O.PEMU, splits=splits)
+        bad = np.abs(o2 - o) > 0.02 + 0.02 * np.abs(o)
+        assert bad.mean() < 0.005
+        assert np.all(np.abs(l2 - l) <= 2.5e-5 + 0.005 * np.abs(l))
+
+
 # ----------------------------------------------------------------------------------------
 # quantisation into the attention inputs (FlashMLA page, 量化 / 解量化的源码实现: scale =
 # amax / 448, stored value e4m3(x / scale); readings in oracle/bsa_oracle.c)

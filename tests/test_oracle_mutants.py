@@ -43,6 +43,11 @@ MUTANTS = {
                               "(double)(float)(p * in->p_scale))) / in->p_scale;"),
     "pemu_exact_p_in_pv": ("tile_acc[k] += pq * oracle_e4m3_decode(vr[k]);",
                            "tile_acc[k] += p * in->p_scale * oracle_e4m3_decode(vr[k]);"),
+    "split_merge_weight_sign": ("double wo = (m == -INFINITY) ? 0.0 : exp(m - mn), wc = exp(mc - mn);",
+                                "double wo = (m == -INFINITY) ? 0.0 : exp(m - mn), wc = exp(mn - mc);"),
+    "split_slice_keeps_earlier_keys": (
+        "    while (a < na && keys[a] < t0) ++a;              /* skip keys of earlier slices */",
+        ""),
     "quant_wrong_max": ("float descale = amax > 0.0f ? amax / 448.0f : 1.0f;",
                         "float descale = amax > 0.0f ? amax / 240.0f : 1.0f;"),
     "quant_zero_row_descale": ("float descale = amax > 0.0f ? amax / 448.0f : 1.0f;",
