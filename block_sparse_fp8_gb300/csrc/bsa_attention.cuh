@@ -37,6 +37,7 @@ constexpr int NTHREADS = 640;        // 4 control warps + 2 pipelines x 2 softma
 constexpr int KSTAGES = 2;
 constexpr int VSTAGES = 2;
 constexpr int KDSTAGES = 2;
+constexpr int MAX_SPLITS = 8;  // split-KV slices per task at most
 constexpr int KD_STRIDE = TILE + 4;
 __host__ __device__ constexpr int kd_index(int token) { return token + (token >= 64 ? 4 : 0); }
 constexpr uint32_t TMEM_COLS = 512;  // per pipeline: S [0, 128), O [128, 256)
@@ -51,7 +52,14 @@ static_assert(SPLIT_REGS <= NTHREADS * 96, "register split must fit 640 threads 
 // so only the last two active tiles of a task can be partly hidden (causal edge, kv_len):
 // the softmax needs just their indices, carried here.
 struct TaskInfo {
-  int b, h, qt, n, q0, q_len, kv_len, tail0, tail1, pad;
+  int b, h, qt;
+  int n;          // tiles of this work item: list positions [lo, lo + n)
+  int q0, q_len, kv_len;
+  int tail0, tail1;  // the task's last two active tiles (the only ones with hidden keys)
+  int lo, ntot;   // first list position of the item, length of the task's whole list
+  int item, task;  // work-item index (task x split) and task index, for split-KV partials
+  int split;       // this item's slice of the task (0 .. splits-1)
+  int pad[2];
 };
 
 struct __align__(1024) Pipe {
@@ -160,22 +168,24 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
                                              const CUtensorMap *tmap_k,
                                              const CUtensorMap *tmap_v) {
   const int lane = threadIdx.x & 31;
-  const int per_qt = p.B * p.N1;
-  const int ntasks = per_qt * p.Qb;
+  const int per_qt = p.B * p.N1 * p.splits;  // work items per Q tile
+  const int nitems = per_qt * p.Qb;
   const int npg = TILE / p.ps;
   int k = 0, qk = 0;
   uint32_t g = 0;
   bool ok = true;
   for (;;) {
-    // claim the next task: tasks are numbered by Q tile, descending, so the longest causal
-    // tasks go first and a pipeline that finishes early takes the next one (longest-first)
+    // claim the next work item: items are numbered by Q tile, descending, so the longest
+    // causal tasks go first and a pipeline that finishes early takes the next one
+    // (longest-first); with split-KV the slices of one task are consecutive items
     int o = 0;
     if (lane == 0) o = atomicAdd(p.task_counter, 1);
     o = __shfl_sync(0xffffffffu, o, 0);
-    if (o >= ntasks) break;
+    if (o >= nitems) break;
     const int qt = p.Qb - 1 - o / per_qt;
     const int rem = o % per_qt;
-    const int b = rem / p.N1, h = rem % p.N1;
+    const int split = rem % p.splits, bh = rem / p.splits;
+    const int b = bh / p.N1, h = bh % p.N1;
     const TaskGeo geo = task_geometry(p, b, qt);
     if (!geo.valid) continue;
     const int slot = k & 1;
@@ -186,7 +196,10 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
     }
     // only this warp reads the list, and it has issued every load of the previous task
     __syncwarp();
-    const int n = compact_task(p, b, h, qt, geo.kend, list, s.bitmap);
+    const int ntot = compact_task(p, b, h, qt, geo.kend, list, s.bitmap);
+    // this item's slice of the task's list, by position (split-KV)
+    const int lo = (int)((long long)split * ntot / p.splits);
+    const int n = (int)((long long)(split + 1) * ntot / p.splits) - lo;
     if (lane == 0) {
       TaskInfo ti;
       ti.b = b;
@@ -196,9 +209,13 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
       ti.q0 = geo.q0;
       ti.q_len = geo.q_len;
       ti.kv_len = geo.kv_len;
-      ti.tail0 = n >= 2 ? list[n - 2] : 0;
-      ti.tail1 = n >= 1 ? list[n - 1] : 0;
-      ti.pad = 0;
+      ti.tail0 = ntot >= 2 ? list[ntot - 2] : 0;
+      ti.tail1 = ntot >= 1 ? list[ntot - 1] : 0;
+      ti.lo = lo;
+      ti.ntot = ntot;
+      ti.item = o;
+      ti.task = (b * p.N1 + h) * p.Qb + qt;
+      ti.split = split;
       s.info[slot] = ti;
       ptx::mbar_arrive(&s.task_full[slot]);
     }
@@ -216,7 +233,7 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
       for (int t = 0; ok && t <= n; ++t) {
         int pgs[4] = {0, 0, 0, 0};
         if (t < n) {
-          const int tile = list[t];
+          const int tile = list[lo + t];
           const int nvalid = tile_pages(p, b, tile, geo.kv_len, pgs);
           const uint32_t gk = g + t;
           const int ks = gk % KSTAGES;
@@ -382,6 +399,100 @@ __device__ __forceinline__ void run_mma(const Params &p, Pipe &s, uint32_t tmem)
 }
 
 // ===================================================================================== softmax
+// Split-KV epilogue of one work item, thread (row r, column half): the item's O half-row
+// (fp32, P-scale units, not normalised) and its (m, l) go to the workspace; the last of the
+// task's items to finish the half-row merges the slices with log-sum-exp weights into the
+// bf16 output, and the half-0 merger writes the LSE (the writes are fenced before the
+// counter, the merger fences after it).  Out of line: it keeps the per-tile loop's register
+// allocation independent of this path.
+__device__ __noinline__ void split_epilogue(const Params &p, Pipe &s, const TaskInfo &ti,
+                                            uint32_t tO, int r, int half, int col0, int n,
+                                            float m, float l_row, float vd, bool row_ok,
+                                            int tok, int h) {
+  const size_t prow = (size_t)ti.item * TILE + r;
+  float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * HEAD_DIM + col0);
+#pragma unroll 1
+  for (int c = 0; c < 2; ++c) {
+    uint32_t o[32];
+    if (n > 0) {
+      ptx::tmem_ld16x2_32<64>(tO + c * 32, o);
+      ptx::tmem_ld_wait(o);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      po[c * 8 + j] = make_float4(u2f(o[4 * j]), u2f(o[4 * j + 1]), u2f(o[4 * j + 2]),
+                                  u2f(o[4 * j + 3]));
+  }
+  reinterpret_cast<float2 *>(p.part_ml)[prow * 2 + half] = make_float2(m, l_row);
+  ptx::tc_fence_before();
+  ptx::mbar_arrive(&s.o_empty);
+  __threadfence();
+  int *cnt = p.row_cnt + ((size_t)ti.task * TILE + r) * 2 + half;
+  if (atomicAdd(cnt, 1) == p.splits - 1) {
+    __threadfence();
+    const size_t row0 = (size_t)(ti.item - ti.split) * TILE + r;  // slice 0 of the task
+    const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
+    float w[MAX_SPLITS];
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < MAX_SPLITS; ++c) {
+      w[c] = 0.f;
+      if (c < p.splits) M = fmaxf(M, __ldcg(&ml[(row0 + (size_t)c * TILE) * 2 + half]).x);
+    }
+    float L = 0.f;
+#pragma unroll
+    for (int c = 0; c < MAX_SPLITS; ++c)
+      if (c < p.splits) {
+        const float2 v = __ldcg(&ml[(row0 + (size_t)c * TILE) * 2 + half]);
+        if (v.x != -INFINITY && v.y > 0.f) {
+          w[c] = ptx::ex2_approx(v.x - M);
+          L += w[c] * v.y;
+        }
+      }
+    const bool any = M != -INFINITY && L > 0.f;
+    const float norm = any ? vd / L : 0.f;
+    uint4 *orow =
+        reinterpret_cast<uint4 *>(p.out + ((size_t)tok * p.N1 + h) * HEAD_DIM + col0);
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {  // 16 columns at a time
+      float acc[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+#pragma unroll
+      for (int c = 0; c < MAX_SPLITS; ++c) {
+        if (c >= p.splits) break;
+        const float wc = w[c] * norm;
+        const float4 *src = reinterpret_cast<const float4 *>(
+            p.part_o + (row0 + (size_t)c * TILE) * HEAD_DIM + col0 + q * 16);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 v = __ldcg(src + j);
+          acc[4 * j] += wc * v.x;
+          acc[4 * j + 1] += wc * v.y;
+          acc[4 * j + 2] += wc * v.z;
+          acc[4 * j + 3] += wc * v.w;
+        }
+      }
+      uint32_t wb[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+        wb[j] = *reinterpret_cast<uint32_t *>(&v2);
+      }
+      if (row_ok) {
+        orow[q * 2] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+        orow[q * 2 + 1] = make_uint4(wb[4], wb[5], wb[6], wb[7]);
+      }
+    }
+    if (half == 0 && row_ok && p.lse)
+      p.lse[(size_t)h * p.T + tok] =
+          any ? (M + __log2f(L)) * 0.69314718055994531f - p.ln_pscale : -3.402823466e38f;
+  }
+}
+
 // Thread (row r, half h) owns columns [64h, 64h + 64) of row r of every tile; `sub` selects
 // which 16 rows of each 32-row TMEM quarter this warpgroup takes.
 __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t tmem, int sub) {
@@ -403,6 +514,8 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
     const TaskInfo &ti = s.info[slot];
     const int n = ti.n;
     if (n < 0) break;
+    // item tiles t >= t_hidden are the task's last two, the only ones with hidden keys
+    const int t_hidden = ti.ntot - 2 - ti.lo;
     float row_scale;
     int causal_lim;  // keys j <= causal_lim are visible to row r
     {
@@ -471,8 +584,8 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
       }
       // hidden keys (past the causal edge or kv_len) take the logit -inf: they neither raise
       // the max nor add to P.  Only the task's last two tiles can hold any.
-      if (t + 2 >= n) {
-        const int tile = (t + 2 == n) ? ti.tail0 : ti.tail1;
+      if (t >= t_hidden) {
+        const int tile = (t == t_hidden) ? ti.tail0 : ti.tail1;
         int lim = ti.kv_len - tile * TILE;  // visible keys of the tile
         if (p.causal) lim = min(lim, causal_lim - tile * TILE + 1);
         lim -= col0;                        // ... of this thread's half
@@ -585,58 +698,62 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
     const bool seen = m != -INFINITY && l_row > 0.f;
     const float vd = p.v_per_head ? p.v_descale[g_kv] : p.v_descale[0];
     const float osc = seen ? vd / l_row : 0.f;
-    const uint64_t osc2 = ptx::pk(osc, osc);
-    // O goes out through this warp's 16 rows of the P tile (PV has finished reading them):
-    // each 32-column round is staged row-wise and copied out so that a store instruction
-    // writes whole 64-byte row segments instead of 16 bytes from each of 32 rows.  Staged
-    // row i holds its two 64-byte segments as chunks 0-3 and 4-7, chunk c at position
-    // c ^ (i % 8) so that both the staging and the copy-out touch every bank once per 128 B.
-    const int r0 = quad * 32 + sub * 16;
-    uint8_t *stage = s.p + r0 * 128;
-    const int i = lane & 15;
-    const int rows_valid = min(TILE, ti.q_len - qt * TILE);
-    uint8_t *orow0 = reinterpret_cast<uint8_t *>(p.out) +
-                     ((size_t)(ti.q0 + qt * TILE + r0) * p.N1 + h) * (HEAD_DIM * 2);
-    const size_t row_bytes = (size_t)p.N1 * HEAD_DIM * 2;
-#pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      uint32_t o[32];
-      if (n > 0) {
-        ptx::tmem_ld16x2_32<64>(tO + c * 32, o);
-        ptx::tmem_ld_wait(o);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = 0u;
+    if (p.splits > 1) {
+      split_epilogue(p, s, ti, tO, r, half, col0, n, m, l_row, vd, row_ok, tok, h);
+    } else {
+      const uint64_t osc2 = ptx::pk(osc, osc);
+      // O goes out through this warp's 16 rows of the P tile (PV has finished reading them):
+      // each 32-column round is staged row-wise and copied out so that a store instruction
+      // writes whole 64-byte row segments instead of 16 bytes from each of 32 rows.  Staged
+      // row i holds its two 64-byte segments as chunks 0-3 and 4-7, chunk c at position
+      // c ^ (i % 8) so that both the staging and the copy-out touch every bank once per 128 B.
+      const int r0 = quad * 32 + sub * 16;
+      uint8_t *stage = s.p + r0 * 128;
+      const int i = lane & 15;
+      const int rows_valid = min(TILE, ti.q_len - qt * TILE);
+      uint8_t *orow0 = reinterpret_cast<uint8_t *>(p.out) +
+                       ((size_t)(ti.q0 + qt * TILE + r0) * p.N1 + h) * (HEAD_DIM * 2);
+      const size_t row_bytes = (size_t)p.N1 * HEAD_DIM * 2;
+  #pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        if (n > 0) {
+          ptx::tmem_ld16x2_32<64>(tO + c * 32, o);
+          ptx::tmem_ld_wait(o);
+        } else {
+  #pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
+        }
+        uint32_t w[16];
+  #pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float a, b3;
+          ptx::upk(ptx::mul2(ptx::pk(u2f(o[2 * j]), u2f(o[2 * j + 1])), osc2), a, b3);
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(a, b3);
+          w[j] = *reinterpret_cast<uint32_t *>(&v2);
+        }
+  #pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4 *>(stage + i * 128 + (((4 * half + q) ^ (i & 7)) << 4)) =
+              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        __syncwarp();
+  #pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int i2 = kk * 4 + (lane >> 3), c8 = lane & 7;
+          const uint4 v = *reinterpret_cast<const uint4 *>(stage + i2 * 128 + ((c8 ^ (i2 & 7)) << 4));
+          if (r0 + i2 < rows_valid)
+            *reinterpret_cast<uint4 *>(orow0 + i2 * row_bytes + (c8 >> 2) * 128 + c * 64 +
+                                       (c8 & 3) * 16) = v;
+        }
+        __syncwarp();
       }
-      uint32_t w[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float a, b3;
-        ptx::upk(ptx::mul2(ptx::pk(u2f(o[2 * j]), u2f(o[2 * j + 1])), osc2), a, b3);
-        __nv_bfloat162 v2 = __floats2bfloat162_rn(a, b3);
-        w[j] = *reinterpret_cast<uint32_t *>(&v2);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&s.o_empty);
+      if (half == 0 && row_ok && p.lse) {
+        const float lse = seen ? (m + __log2f(l_row)) * 0.69314718055994531f - p.ln_pscale
+                               : -3.402823466e38f;
+        p.lse[(size_t)h * p.T + tok] = lse;
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4 *>(stage + i * 128 + (((4 * half + q) ^ (i & 7)) << 4)) =
-            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-      __syncwarp();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int i2 = kk * 4 + (lane >> 3), c8 = lane & 7;
-        const uint4 v = *reinterpret_cast<const uint4 *>(stage + i2 * 128 + ((c8 ^ (i2 & 7)) << 4));
-        if (r0 + i2 < rows_valid)
-          *reinterpret_cast<uint4 *>(orow0 + i2 * row_bytes + (c8 >> 2) * 128 + c * 64 +
-                                     (c8 & 3) * 16) = v;
-      }
-      __syncwarp();
-    }
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(&s.o_empty);
-    if (half == 0 && row_ok && p.lse) {
-      const float lse = seen ? (m + __log2f(l_row)) * 0.69314718055994531f - p.ln_pscale
-                             : -3.402823466e38f;
-      p.lse[(size_t)h * p.T + tok] = lse;
     }
     ptx::mbar_arrive(&s.task_empty[slot]);
     g += n;

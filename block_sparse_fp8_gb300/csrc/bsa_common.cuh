@@ -28,7 +28,14 @@ struct Params {
   __nv_bfloat16 *out;
   float *lse;
   int *dev_status;
-  int *task_counter;  // zeroed before launch; CTAs claim task indices from it
+  int *task_counter;  // zeroed before launch; CTAs claim work-item indices from it
+  // split-KV (splits > 1): per work item and row, the un-normalised O (fp32 [item][128][128])
+  // and (m, l) per row half ([item][128][2] float2); per task, row and half a counter of the
+  // items done (zeroed before launch)
+  int splits;
+  float *part_o;
+  float *part_ml;
+  int *row_cnt;
   int B, N1, N2, G, ps, max_q_len, max_kv_len, num_pages, L, T, Qb, Kb;
   int k_per_token, v_per_head, causal;
   int q_ntd, kv_nhd;  // layouts: Q [N1, T, 128] (q_descale [N1, T]); pages [P, ps, N2, 128]

@@ -189,12 +189,48 @@ static bool encode_map(CUtensorMap *map, const void *base, int rank, const cuuin
 
 using namespace bsa;
 
-// one int: the task counter the persistent CTAs claim work from (padded to 256 bytes)
+// one int: the work-item counter the persistent CTAs claim work from (padded to 256 bytes)
 static constexpr size_t WORKSPACE_BYTES = 256;
+
+namespace {
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Split-KV plan.  When the (b, h, q-tile) tasks cannot occupy half of the pipelines (two per
+// SM), each task's active list is cut into S slices (work items) that run on separate
+// pipelines and are merged afterwards.  S = min(8, pipelines / tasks, Kb / 16): a slice covers
+// at least 16 KV tiles of the task's range.  Splitting costs a partial write and a merge per
+// task, which measured more than it saved once every pipeline already had a task.
+struct SplitPlan {
+  int splits = 1;
+  size_t bytes = WORKSPACE_BYTES;           // workspace needed
+  size_t off_cnt = 0, off_ml = 0, off_o = 0;
+};
+
+SplitPlan plan_splits(const Params &p, int num_sms, bool allow) {
+  SplitPlan plan;
+  const long long ntasks = (long long)p.B * p.N1 * p.Qb;
+  const long long pipes = (long long)attn::NPIPE * std::max(num_sms, 1);
+  if (!allow || ntasks <= 0 || 2 * ntasks > pipes) return plan;
+  const int best = (int)std::min<long long>(std::min<long long>(attn::MAX_SPLITS, pipes / ntasks),
+                                             p.Kb / 16);
+  if (best <= 1) return plan;
+  const long long items = ntasks * best;
+  plan.splits = best;
+  plan.off_cnt = WORKSPACE_BYTES;
+  plan.off_ml = plan.off_cnt + round256((size_t)ntasks * TILE * 2 * sizeof(int));
+  plan.off_o = plan.off_ml + round256((size_t)items * TILE * 2 * 2 * sizeof(float));
+  plan.bytes = plan.off_o + (size_t)items * TILE * HEAD_DIM * sizeof(float);
+  return plan;
+}
+
+}  // namespace
 
 extern "C" size_t bsa_fp8_prefill_workspace_size(const bsa_fp8_dims_t *dims) {
   if (validate_dims(dims) != BSA_OK) return 0;
-  return WORKSPACE_BYTES;
+  int num_sms = 0;
+  if (check_device(0, &num_sms) != BSA_OK) return WORKSPACE_BYTES;
+  return plan_splits(make_params(dims), num_sms, true).bytes;
 }
 
 extern "C" const char *bsa_status_string(bsa_status_t status) {
@@ -235,16 +271,17 @@ extern "C" bsa_status_t bsa_fp8_compact_tiles(const bsa_fp8_dims_t *dims, const 
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
-extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *q,
-                                        const void *k_pages, const void *v_pages,
-                                        const float *q_descale, const float *k_descale,
-                                        const float *v_descale, const int *cu_seqlens_q,
-                                        const int *seqused_kv, const int *block_table,
-                                        const uint8_t *block_mask, const int *sparse_indices,
-                                        const int *sparse_seq_len, float softmax_scale,
-                                        float p_scale, void *out_bf16, float *lse_f32,
-                                        void *workspace, size_t workspace_bytes,
-                                        int *dev_status, void *stream) {
+// The prefill; `allow_split` lets it use split-KV when the plan asks for it (the workspace must
+// then hold the plan's bytes).
+static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, const void *k_pages,
+                                 const void *v_pages, const float *q_descale,
+                                 const float *k_descale, const float *v_descale,
+                                 const int *cu_seqlens_q, const int *seqused_kv,
+                                 const int *block_table, const uint8_t *block_mask,
+                                 const int *sparse_indices, const int *sparse_seq_len,
+                                 float softmax_scale, float p_scale, void *out_bf16,
+                                 float *lse_f32, void *workspace, size_t workspace_bytes,
+                                 int *dev_status, void *stream, bool allow_split) {
   bsa_status_t st = validate_dims(dims);
   if (st != BSA_OK) return st;
   if (block_mask && sparse_indices) return BSA_ERR_INVALID_ARGUMENT;
@@ -269,6 +306,17 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
   int num_sms = 0, per_sm = 1;
   st = check_device(smem, &num_sms, &per_sm);
   if (st != BSA_OK) return st;
+  const SplitPlan plan = plan_splits(p, num_sms, allow_split);
+  if (workspace_bytes < plan.bytes ||
+      (plan.splits > 1 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return BSA_ERR_WORKSPACE;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  p.splits = plan.splits;
+  if (plan.splits > 1) {
+    p.row_cnt = reinterpret_cast<int *>(ws + plan.off_cnt);
+    p.part_ml = reinterpret_cast<float *>(ws + plan.off_ml);
+    p.part_o = reinterpret_cast<float *>(ws + plan.off_o);
+  }
 
   p.q_descale = q_descale;
   p.k_descale = k_descale;
@@ -318,13 +366,32 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
     if (!encode_map(&tk, k_pages, 4, gd, gs, box)) return BSA_ERR_CUDA;
     if (!encode_map(&tv, v_pages, 4, gd, gs, box)) return BSA_ERR_CUDA;
   }
-  // persistent grid: one CTA per SM
-  const long long grid = std::min<long long>(ntasks, (long long)per_sm * num_sms);
-  if (cudaMemsetAsync(workspace, 0, sizeof(int), (cudaStream_t)stream) != cudaSuccess)
+  // persistent grid: one CTA per SM (two pipelines each)
+  const long long items = ntasks * plan.splits;
+  const long long grid = std::min<long long>(items, (long long)per_sm * num_sms);
+  // the item counter, and with split-KV the per-row completion counters, start at zero
+  const size_t zero_bytes = plan.splits > 1 ? plan.off_ml : sizeof(int);
+  if (cudaMemsetAsync(workspace, 0, zero_bytes, (cudaStream_t)stream) != cudaSuccess)
     return BSA_ERR_CUDA;
   attn::bsa_attention_kernel<<<(unsigned)grid, attn::NTHREADS, smem, (cudaStream_t)stream>>>(
       p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *q,
+                                        const void *k_pages, const void *v_pages,
+                                        const float *q_descale, const float *k_descale,
+                                        const float *v_descale, const int *cu_seqlens_q,
+                                        const int *seqused_kv, const int *block_table,
+                                        const uint8_t *block_mask, const int *sparse_indices,
+                                        const int *sparse_seq_len, float softmax_scale,
+                                        float p_scale, void *out_bf16, float *lse_f32,
+                                        void *workspace, size_t workspace_bytes,
+                                        int *dev_status, void *stream) {
+  return prefill_impl(dims, q, k_pages, v_pages, q_descale, k_descale, v_descale, cu_seqlens_q,
+                      seqused_kv, block_table, block_mask, sparse_indices, sparse_seq_len,
+                      softmax_scale, p_scale, out_bf16, lse_f32, workspace, workspace_bytes,
+                      dev_status, stream, true);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -457,13 +524,13 @@ extern "C" bsa_status_t bsa_fp8_prefill_noalloc(
     const uint8_t *block_mask, const int *sparse_indices, const int *sparse_seq_len,
     float softmax_scale, float p_scale, void *out_bf16, float *lse_f32, int *dev_status,
     void *stream) {
-  // the array is a fixed 256 bytes: a problem needing more workspace is refused, not truncated
-  if (bsa_fp8_prefill_workspace_size(dims) > NOALLOC_SCRATCH_BYTES) return BSA_ERR_WORKSPACE;
+  // the array is a fixed 256 bytes, all the unsplit prefill needs
   void *scratch = nullptr;
   const bsa_status_t st = noalloc_scratch(&scratch);
   if (st != BSA_OK) return st;
-  return bsa_fp8_prefill(dims, q, k_pages, v_pages, q_descale, k_descale, v_descale,
-                         cu_seqlens_q, seqused_kv, block_table, block_mask, sparse_indices,
-                         sparse_seq_len, softmax_scale, p_scale, out_bf16, lse_f32, scratch,
-                         NOALLOC_SCRATCH_BYTES, dev_status, stream);
+  // the array holds the item counter only: this entry point never splits the KV lists
+  return prefill_impl(dims, q, k_pages, v_pages, q_descale, k_descale, v_descale, cu_seqlens_q,
+                      seqused_kv, block_table, block_mask, sparse_indices, sparse_seq_len,
+                      softmax_scale, p_scale, out_bf16, lse_f32, scratch, NOALLOC_SCRATCH_BYTES,
+                      dev_status, stream, false);
 }

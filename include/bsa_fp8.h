@@ -103,10 +103,15 @@ typedef struct {
 #define BSA_KV_HND 0
 #define BSA_KV_NHD 1
 
-/* Bytes of device workspace bsa_fp8_prefill needs for `dims` (currently 256: the counter
- * the persistent kernel's CTAs claim tasks from; bsa_fp8_prefill zeroes it on `stream`
- * before each launch, so two calls in flight at once must not share one workspace).
- * Returns 0 for invalid dims; bsa_fp8_prefill reports those. */
+/* Bytes of device workspace bsa_fp8_prefill needs for `dims` on the current device: 256 (the
+ * counter the persistent kernel's CTAs claim work items from) when every SM pipeline gets a
+ * (b, h, q-tile) task; when the tasks cannot occupy half of the pipelines, the prefill cuts
+ * each task's active list into up to 8 slices (split-KV) and the workspace also holds, per
+ * slice, the un-normalised fp32 O [128, 128] and (m, l) of each row half, plus a counter per
+ * task row and half (about 65 KB per slice).  bsa_fp8_prefill zeroes the counters on
+ * `stream` before each launch, so two calls in flight at once must not share one workspace;
+ * a split plan needs a 256-byte aligned workspace.  Returns 0 for invalid dims;
+ * bsa_fp8_prefill reports those. */
 size_t bsa_fp8_prefill_workspace_size(const bsa_fp8_dims_t *dims);
 
 /* Block-sparse FP8 attention prefill over a paged KV cache.
@@ -172,9 +177,9 @@ bsa_status_t bsa_fp8_compact_tiles(const bsa_fp8_dims_t *dims, const int *cu_seq
  * those 256 bytes until the process exits).
  *
  *   - Arguments, layouts, results and errors are exactly those of bsa_fp8_prefill, minus
- *     `workspace` / `workspace_bytes`.  A problem whose workspace need
- *     (bsa_fp8_prefill_workspace_size) exceeds the 256-byte array is rejected with
- *     BSA_ERR_WORKSPACE; today every valid problem needs 256 bytes or less.
+ *     `workspace` / `workspace_bytes`.  It never uses split-KV, so every valid problem fits
+ *     the 256-byte array; a problem for which bsa_fp8_prefill would split runs unsplit here
+ *     (the same result up to the rounding of P against each slice's own running max).
  *   - The first call on a device (with that device current) looks up the array's device
  *     address once; make that first call before any stream capture.  Failure of the lookup
  *     is BSA_ERR_CUDA.

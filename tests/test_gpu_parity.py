@@ -267,21 +267,24 @@ def test_workload_parity(name):
     out, lse, st = run(case, d)
     assert st == 0
     orc = O.Oracle(case)
+    # few long-KV tasks (the chunked workload) run split-KV: emulate the same slices
+    S = _expected_splits(case, torch.cuda.get_device_properties(0).multi_processor_count)
     rows = sample_rows(case, 1536 if case.T > 4096 else case.T * case.N1, seed=7)
     if case.T * case.N1 <= 65536:
         o_ex, l_ex, _ = orc.all_rows(O.EXACT)
-        o_pe, _, _ = orc.all_rows(O.PEMU)
+        o_pe, _, _ = orc.all_rows(O.PEMU, splits=S)
         got = out.float().cpu().numpy()
         gl = lse.cpu().numpy()
     else:
         o_ex, l_ex, _ = orc.rows(rows, O.EXACT)
-        o_pe, _, _ = orc.rows(rows, O.PEMU)
+        o_pe, _, _ = orc.rows(rows, O.PEMU, splits=S)
         got = out.float()[rows[:, 0], rows[:, 1]].cpu().numpy()
         gl = lse[rows[:, 1], rows[:, 0]].cpu().numpy()
     check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, f"{name} vs exact")
-    check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, f"{name} vs P-emulating")
+    check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, f"{name} vs P-emulating ({S} slice(s))")
     check_lse(gl, l_ex, f"{name} lse")
-    # every task is computed by one CTA in a fixed order: repeated runs agree bit for bit
+    # every task (or slice) is computed by one pipeline in a fixed order and slices merge in a
+    # fixed order: repeated runs agree bit for bit
     o_again, l_again, st = run(case, d)
     assert st == 0 and torch.equal(out, o_again) and torch.equal(lse, l_again)
     if case.block_mask is None and case.sparse_indices is None:
@@ -321,3 +324,52 @@ def test_layouts_q_ntd_and_kv_nhd(name):
         assert st == 0
         assert torch.equal(out, base), f"layout ({ql}, {kl}) changed O"
         assert torch.equal(lse, base_lse), f"layout ({ql}, {kl}) changed LSE"
+
+
+def _expected_splits(case, num_sms):
+    """The library's split-KV plan (restated): split only when the tasks cannot occupy half
+    of the pipelines (two per SM); then S = min(8, pipelines // tasks, Kb // 16)."""
+    ntasks = case.B * case.N1 * case.Qb
+    pipes = 2 * num_sms
+    if 2 * ntasks > pipes:
+        return 1
+    return max(1, min(8, pipes // ntasks, case.Kb // 16))
+
+
+SPLIT_CASES = {
+    "split_long_kv": dict(seed=201, q_lens=[256], kv_lens=[8229], N1=2, N2=1, page_size=64,
+                          k_scale_kind=1, v_scale_kind=2, mask="bernoulli", keep=0.5),
+    "split_chunked": dict(seed=202, q_lens=[384], kv_lens=[16384], N1=4, N2=2, page_size=32,
+                          k_scale_kind=1, v_scale_kind=2, mask="local_sink", n_local=2,
+                          p_far=0.3),
+    "split_dense_noncausal": dict(seed=203, q_lens=[130, 70], kv_lens=[9000, 8300], N1=2,
+                                  N2=2, page_size=64, mask="none", causal=0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SPLIT_CASES))
+def test_split_kv_parity(name):
+    """Few long-KV tasks: the prefill cuts each task's list into S slices (work items) and
+    merges them; the result matches the oracle's P-emulating mode with the same slices (tight
+    band) and the exact result (exact band), row by row, LSE included."""
+    import block_sparse_fp8_gb300 as bsa
+
+    case = W.make_case(name, **SPLIT_CASES[name])
+    S = _expected_splits(case, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert S > 1, "the case is meant to split"
+    ws = bsa.workspace_size(bsa.Dims(**case.dims()))
+    items = case.B * case.N1 * case.Qb * S
+    assert ws >= 256 + items * 128 * 128 * 4, "workspace does not hold the split partials"
+    out, lse, st = run(case)
+    assert st == 0
+    got = out.float().cpu().numpy()
+    a = O.Oracle(case)
+    o_ex, l_ex, err = a.all_rows(O.EXACT)
+    o_pe, l_pe, _ = a.all_rows(O.PEMU, splits=S)
+    assert err == 0
+    check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, f"{name} vs exact")
+    check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, f"{name} vs P-emulating, {S} slices")
+    check_lse(lse.cpu().numpy(), l_pe, f"{name} LSE")
+    # run twice: the partials and counters are re-initialised per call
+    out2, lse2, st2 = run(case)
+    assert st2 == 0 and torch.equal(out2, out) and torch.equal(lse2, lse)

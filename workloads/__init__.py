@@ -386,6 +386,10 @@ WORKLOADS = {
     "dense_32k_h32kv8": dict(
         seed=1005, q_lens=[32768], kv_lens=[32768], N1=32, N2=8, page_size=64,
         k_scale_kind=SCALE_PER_TOKEN_HEAD, v_scale_kind=SCALE_PER_HEAD, mask="none"),
+    # few tasks over a long KV (32 tasks for 304 pipelines): the split-KV regime
+    "short_q_512_over_64k_h8kv1_dense": dict(
+        seed=1006, q_lens=[512], kv_lens=[65536], N1=8, N2=1, page_size=64,
+        k_scale_kind=SCALE_PER_TOKEN_HEAD, v_scale_kind=SCALE_PER_HEAD, mask="none"),
 }
 
 WORKLOAD_ORDER = list(WORKLOADS)
