@@ -71,6 +71,25 @@ def peaks():
         return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of a list of floats over the ranks of the default process group
+    (the slowest replica sets the time); the values themselves with one rank."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def weak_scaling_value(world, work_per_replica, ms):
+    """Whole-job throughput of `world` replicas each doing `work_per_replica` units in `ms`
+    (the maximum over ranks): total units per second."""
+    return world * work_per_replica / (ms * 1e-3)
+
+
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "bsa_attention_kernel__dram_traffic.json")
 # the attention kernel's device code (its launch shape is fixed: one 640-thread CTA per SM)
 KERNEL_SOURCES = ("bsa_attention.cuh", "bsa_common.cuh", "ptx_sm103.cuh")
@@ -308,10 +327,7 @@ def run_ours(args, rank, world):
     clocks = sampler.stop() if sampler else None
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(per) / len(per)
-    if world > 1:
-        tt = torch.tensor([ms, wall], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms, wall = float(tt[0]), float(tt[1])
+    ms, wall = max_over_ranks([ms, wall], dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the timed region")
 
@@ -376,11 +392,8 @@ def run_ours(args, rank, world):
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = ev0.elapsed_time(ev1) / n_e2e
-        if world > 1:
-            tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(tt[0])
-        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e_ms = max_over_ranks([e2e_ms], dev)[0]
+        e2e = {"value": weak_scaling_value(world, flops, e2e_ms) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms}
 
@@ -390,7 +403,8 @@ def run_ours(args, rank, world):
     fp8_peak = pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS) * FP8_PER_BF16
     achieved = flops / (ms * 1e-3) / 1e12
     line = {
-        "metric": METRIC, "value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "metric": METRIC, "value": weak_scaling_value(world, flops, ms) / 1e12,
+        "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic (seeded)",
@@ -540,11 +554,7 @@ def run_quantize(args, rank, world):
         e1.record()
         torch.cuda.synchronize()
         per.append(e0.elapsed_time(e1))
-    ms = statistics.mean(per)
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt[0])
+    ms = max_over_ranks([statistics.mean(per)], dev)[0]
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
     if rank != 0:
@@ -555,7 +565,8 @@ def run_quantize(args, rank, world):
     return {
         "metric": "quantise step (bf16 Q rows -> e4m3 + descale, K/V append into pages) "
                   "HBM throughput",
-        "value": world * achieved, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "value": weak_scaling_value(world, nbytes, ms) / 1e9, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 -> fp8_e4m3",
         "data": "synthetic (seeded normal)",

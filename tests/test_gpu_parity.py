@@ -373,3 +373,27 @@ def test_split_kv_parity(name):
     # run twice: the partials and counters are re-initialised per call
     out2, lse2, st2 = run(case)
     assert st2 == 0 and torch.equal(out2, out) and torch.equal(lse2, lse)
+
+
+def test_longest_supported_kv():
+    """Kb = 4096 KV tiles (524,288 keys): the longest list the kernel holds in shared memory.
+    Four tasks, so the prefill also splits; lists bit-exact, sampled rows against the oracle."""
+    case = W.make_case("max_kb", 301, [256], [4096 * 128], 2, 1, 64, W.SCALE_PER_TOKEN_HEAD,
+                       W.SCALE_PER_HEAD, "local_sink", n_local=2, p_far=0.01)
+    assert case.Kb == 4096
+    d = to_device(case)
+    ref_l, ref_c, _ = O.Oracle(case).lists()
+    lists, counts, st = run_lists(case, d)
+    assert st == 0 and np.array_equal(counts, ref_c) and np.array_equal(lists, ref_l)
+    out, lse, st = run(case, d)
+    assert st == 0
+    S = _expected_splits(case, torch.cuda.get_device_properties(0).multi_processor_count)
+    rows = sample_rows(case, 96, seed=3)
+    orc = O.Oracle(case)
+    o_ex, l_ex, err = orc.rows(rows, O.EXACT)
+    o_pe, _, _ = orc.rows(rows, O.PEMU, splits=S)
+    assert err == 0
+    got = out.float()[rows[:, 0], rows[:, 1]].cpu().numpy()
+    check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, "max Kb vs exact")
+    check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, f"max Kb vs P-emulating ({S} slices)")
+    check_lse(lse[rows[:, 1], rows[:, 0]].cpu().numpy(), l_ex, "max Kb lse")
