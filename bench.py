@@ -402,6 +402,12 @@ def run_ours(args, rank, world):
     pk, src = peaks()
     fp8_peak = pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS) * FP8_PER_BF16
     achieved = flops / (ms * 1e-3) / 1e12
+    traffic = measured_traffic(args.workload) if args.batch == 0 else None
+    hbm_peak = pk.get("hbm_gbs", 6800.0)
+    hbm = None if traffic is None else {
+        "achieved": traffic / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+        "frac": traffic / (ms * 1e-3) / 1e9 / hbm_peak,
+        "note": "recorded DRAM bytes per launch over the measured launch time"}
     line = {
         "metric": METRIC, "value": weak_scaling_value(world, flops, ms) / 1e12,
         "unit": "TFLOP/s",
@@ -412,8 +418,8 @@ def run_ours(args, rank, world):
         "ms_per_call": {"mean": ms, "median": statistics.median(per), "min": min(per)},
         "wall_ms_per_step_incl_flush": wall * 1e3 / args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak,
-                     "unit": "TFLOP/s", "frac": achieved / fp8_peak,
-                     "traffic": measured_traffic(args.workload) if args.batch == 0 else None,
+                     "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": traffic,
+                     "hbm": hbm,
                      "peak_source": f"{src}: bf16 {'burst' if src == 'measured' else ''} "
                                     f"{pk.get('bf16_tflops')} TFLOP/s x {FP8_PER_BF16} "
                                     f"(nominal fp8/bf16 ratio)",
