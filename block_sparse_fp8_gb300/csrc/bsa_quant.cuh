@@ -124,20 +124,16 @@ struct AppendParams {
   int k_per_token, v_per_head, kv_nhd;
 };
 
+// One warp per new token: lane 0 finds the token's sequence and page once, then the two
+// half-warps take two heads at a time, each with its K and V rows in flight together.
 __global__ void __launch_bounds__(THREADS) append_kv_kernel(const AppendParams p) {
-  const int lane = threadIdx.x & 15;
-  const long long rows = (long long)p.total_new * p.N2;
-  const long long step = (long long)gridDim.x * (THREADS / 16);
-  const long long first = (long long)blockIdx.x * (THREADS / 16) + (threadIdx.x >> 4);
-  const long long iters = (rows + step - 1) / step;
-  for (long long it = 0; it < iters; ++it) {
-    const long long r = first + it * step;
-    bool live = r < rows;
-    long long dst = 0, row = 0;  // descale index and 128-byte page row of the token
-    int g = 0;
-    if (live) {
-      const int tok = (int)(r / p.N2);
-      g = (int)(r % p.N2);
+  const int lane = threadIdx.x & 31, hl = lane & 15, hw = lane >> 4;
+  const int warps = gridDim.x * (THREADS / 32);
+  for (int tok = blockIdx.x * (THREADS / 32) + (threadIdx.x >> 5); tok < p.total_new;
+       tok += warps) {
+    long long slot = 0;
+    int pg = -1;
+    if (lane == 0) {
       // sequence of the token: the last b with cu_new[b] <= tok
       int lo = 0, hi = p.B - 1;
       while (lo < hi) {
@@ -146,29 +142,36 @@ __global__ void __launch_bounds__(THREADS) append_kv_kernel(const AppendParams p
       }
       const long long pos = (long long)p.cache_len[lo] + (tok - p.cu_new[lo]);
       const long long lp = pos / p.ps;
-      const int pg = (pos >= 0 && lp < p.L) ? p.block_table[(size_t)lo * p.L + lp] : -1;
+      pg = (pos >= 0 && lp < p.L) ? p.block_table[(size_t)lo * p.L + lp] : -1;
       if (pg < 0 || pg >= p.num_pages) {
-        if (lane == 0) report_status(p.dev_status, BSA_DEV_BAD_PAGE);
-        live = false;
+        report_status(p.dev_status, BSA_DEV_BAD_PAGE);
+        pg = -1;
       } else {
-        const long long slot = pos % p.ps;
-        dst = ((long long)pg * p.N2 + g) * p.ps + slot;  // the K descale's index [P, N2, ps]
-        row = p.kv_nhd ? ((long long)pg * p.ps + slot) * p.N2 + g : dst;
+        slot = pos % p.ps;
       }
     }
-    // K and V rows both in flight before either is used
-    const uint4 wk = live ? p.k_new[r * 16 + lane] : make_uint4(0, 0, 0, 0);
-    const uint4 wv = live ? p.v_new[r * 16 + lane] : make_uint4(0, 0, 0, 0);
-    float v[8];
-    unpack8(wk, v);
-    // the shuffles of row_amax run on every lane, live or not
-    const float amax = row_amax(v);
-    if (live) {
-      const float d = p.k_per_token ? descale_of(amax) : p.k_scale[0];
-      p.k_pages[row * 16 + lane] = codes8(v, d);
-      if (p.k_per_token && lane == 0) p.k_descale[dst] = d;
-      unpack8(wv, v);
-      p.v_pages[row * 16 + lane] = codes8(v, p.v_per_head ? p.v_scale[g] : p.v_scale[0]);
+    pg = __shfl_sync(0xffffffffu, pg, 0);
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    if (pg < 0) continue;  // warp-uniform
+    for (int g0 = 0; g0 < p.N2; g0 += 2) {
+      const int g = g0 + hw;
+      const bool live = g < p.N2;
+      const long long r = (long long)tok * p.N2 + g;
+      const long long dst = ((long long)pg * p.N2 + g) * p.ps + slot;  // K descale index
+      const long long row = p.kv_nhd ? ((long long)pg * p.ps + slot) * p.N2 + g : dst;
+      const uint4 wk = live ? p.k_new[r * 16 + hl] : make_uint4(0, 0, 0, 0);
+      const uint4 wv = live ? p.v_new[r * 16 + hl] : make_uint4(0, 0, 0, 0);
+      float v[8];
+      unpack8(wk, v);
+      // the shuffles of row_amax run on every lane, live or not
+      const float amax = row_amax(v);
+      if (live) {
+        const float d = p.k_per_token ? descale_of(amax) : p.k_scale[0];
+        p.k_pages[row * 16 + hl] = codes8(v, d);
+        if (p.k_per_token && hl == 0) p.k_descale[dst] = d;
+        unpack8(wv, v);
+        p.v_pages[row * 16 + hl] = codes8(v, p.v_per_head ? p.v_scale[g] : p.v_scale[0]);
+      }
     }
   }
 }
