@@ -41,7 +41,6 @@ constexpr int MAX_SPLITS = 8;  // split-KV slices per task at most
 constexpr int KD_STRIDE = TILE + 4;
 __host__ __device__ constexpr int kd_index(int token) { return token + (token >= 64 ? 4 : 0); }
 constexpr uint32_t TMEM_COLS = 512;  // per pipeline: S [0, 128), O [128, 256)
-constexpr bool POLY_EXP = false;     // part of exp2 on the FMA pipe (see exp2_poly2); measured slower
 constexpr int CTRL_REGS = 56;
 constexpr int SOFTMAX_REGS = 104;
 // registers the split needs from the launch allocation (640 threads x 96 = 61440)
@@ -621,16 +620,8 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
           float e0, e1, e2, e3;
           ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j]), u2f(x[c][j + 1])), rs2, b2), e0, e1);
           ptx::upk(ptx::fma2(ptx::pk(u2f(x[c][j + 2]), u2f(x[c][j + 3])), rs2, b2), e2, e3);
-          float p0, p1, p2, p3;
-          if (POLY_EXP && p.poly_exp && ((c * 8 + (j >> 2)) % 3) == 2) {
-            ptx::exp2_poly2(e0, e1, p0, p1);
-            ptx::exp2_poly2(e2, e3, p2, p3);
-          } else {
-            p0 = ptx::ex2_approx(e0);
-            p1 = ptx::ex2_approx(e1);
-            p2 = ptx::ex2_approx(e2);
-            p3 = ptx::ex2_approx(e3);
-          }
+          const float p0 = ptx::ex2_approx(e0), p1 = ptx::ex2_approx(e1);
+          const float p2 = ptx::ex2_approx(e2), p3 = ptx::ex2_approx(e3);
           acc0 = ptx::add2(acc0, ptx::pk(p0, p1));
           acc1 = ptx::add2(acc1, ptx::pk(p2, p3));
           packed[(c * 32 + j) >> 2] = ptx::cvt_e4m3x4(p0, p1, p2, p3);

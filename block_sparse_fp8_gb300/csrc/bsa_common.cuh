@@ -40,7 +40,6 @@ struct Params {
   int k_per_token, v_per_head, causal;
   int q_ntd, kv_nhd;  // layouts: Q [N1, T, 128] (q_descale [N1, T]); pages [P, ps, N2, 128]
   int qd_tok, qd_head;  // q_descale element strides of a token and of a head
-  int poly_exp;       // 1: part of exp2 by polynomial (safe for the p_scale in use)
   float scale_log2;   // softmax_scale * log2(e)
   float log2_pscale;  // log2(p_scale)
   float ln_pscale;    // ln(p_scale)

@@ -334,8 +334,6 @@ static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, cons
   p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
   p.log2_pscale = (float)std::log2((double)p_scale);
   p.ln_pscale = (float)std::log((double)p_scale);
-  // the clamped polynomial exp2 is only used where its input range is safe
-  p.poly_exp = (p.log2_pscale <= 64.f && p.log2_pscale >= -32.f) ? 1 : 0;
 
   // Tensor maps, innermost dimension first.  Either layout puts one 128-token Q box of a head,
   // or one page of a KV head, into shared memory as consecutive 128-byte rows.

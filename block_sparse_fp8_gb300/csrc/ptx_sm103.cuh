@@ -262,35 +262,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-__device__ __forceinline__ float min3(float a, float b, float c) {
-  float d;
-  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// 2^e for two lanes without the MUFU unit.  Cody-Waite reduction: n = round(e) through the
-// fp32 magic number 1.5 * 2^23, f = e - n in [-1/2, 1/2]; 2^f from a degree-4 polynomial with
-// minimax relative error 2.7e-6 (coefficients from fit_exp2_poly.py, Remez exchange); 2^n is
-// applied by adding n << 23 to the exponent field.  Inputs below -126 are clamped to -126 so
-// the exponent never wraps (2^-126 is far below anything the e4m3 P or the row sum can see).
-__device__ __forceinline__ void exp2_poly2(float e0, float e1, float &p0, float &p1) {
-  const uint64_t magic = pk(12582912.f, 12582912.f);
-  const uint64_t neg_magic = pk(-12582912.f, -12582912.f);
-  const uint64_t minus1 = pk(-1.f, -1.f);
-  const uint64_t e = pk(fmaxf(e0, -126.f), fmaxf(e1, -126.f));
-  const uint64_t j = add2(e, magic);
-  const uint64_t n = add2(j, neg_magic);
-  const uint64_t f = fma2(n, minus1, e);
-  uint64_t q = fma2(pk(0x1.3997d6p-7f, 0x1.3997d6p-7f), f, pk(0x1.ca1440p-5f, 0x1.ca1440p-5f));
-  q = fma2(q, f, pk(0x1.ec06dap-3f, 0x1.ec06dap-3f));
-  q = fma2(q, f, pk(0x1.62e0dcp-1f, 0x1.62e0dcp-1f));
-  q = fma2(q, f, pk(0x1.ffffe8p-1f, 0x1.ffffe8p-1f));
-  float q0, q1, j0, j1;
-  upk(q, q0, q1);
-  upk(j, j0, j1);
-  p0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(j0) << 23));
-  p1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(j1) << 23));
-}
 
 // ------------------------------------------------------------------ register reallocation
 template <uint32_t N>
