@@ -88,7 +88,9 @@ static bsa_status_t validate_dims(const bsa_fp8_dims_t *d) {
   if (d->q_layout != BSA_Q_TND && d->q_layout != BSA_Q_NTD) return BSA_ERR_INVALID_ARGUMENT;
   if (d->kv_layout != BSA_KV_HND && d->kv_layout != BSA_KV_NHD) return BSA_ERR_INVALID_ARGUMENT;
   if (cdiv(d->max_kv_len, TILE) > KB_MAX) return BSA_ERR_UNSUPPORTED;
-  if ((long long)d->B * d->N1 * cdiv(d->max_q_len, TILE) > 0x7fffffffLL)
+  // task indices are int; the work-item counter runs past the last task by up to one claim
+  // per pipeline, so keep the count well inside int range
+  if ((long long)d->B * d->N1 * cdiv(d->max_q_len, TILE) > (1LL << 30))
     return BSA_ERR_UNSUPPORTED;
   return BSA_OK;
 }
@@ -297,7 +299,8 @@ static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, cons
     return BSA_ERR_INVALID_ARGUMENT;
   if (p.num_pages < 1 || p.L < 1) return BSA_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) ||
-      (p.k_per_token && !aligned16(k_descale)) || !aligned16(out_bf16))
+      (p.k_per_token && !aligned16(k_descale)) || !aligned16(out_bf16) ||
+      (reinterpret_cast<uintptr_t>(lse_f32) & 3u) != 0)
     return BSA_ERR_INVALID_ARGUMENT;
   if (!workspace || workspace_bytes < WORKSPACE_BYTES ||
       (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)

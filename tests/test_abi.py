@@ -80,6 +80,12 @@ def test_too_many_kv_tiles_unsupported(L):
     assert _prefill(L, d) == UNSUPPORTED
 
 
+def test_too_many_tasks_unsupported(L):
+    # B * N1 * Qb above 2^30: the int work-item counter must not wrap
+    d = _dims(B=1 << 12, N1=16, N2=1, max_q_len=(1 << 14) * 128 + 1)
+    assert _prefill(L, d) == UNSUPPORTED
+
+
 def test_invalid_scalars_and_pointers(L):
     d = _dims()
     assert _prefill(L, d, scale=float("inf")) == INVALID
@@ -92,6 +98,7 @@ def test_invalid_scalars_and_pointers(L):
         assert _prefill(L, d, **{k: None}) == INVALID, k
     assert _prefill(L, d, q=0x10001) == INVALID     # TMA needs 16-byte aligned bases
     assert _prefill(L, d, k=0x10008) == INVALID
+    assert _prefill(L, d, lse=0x10002) == INVALID   # fp32 LSE needs 4-byte alignment
     assert _prefill(L, _dims(num_pages=0)) == INVALID
 
 
