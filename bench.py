@@ -639,9 +639,6 @@ def run_quantize(args, rank, world):
                    "v_scale": "per_head", "bytes_per_step": nbytes,
                    "l2": "flushed (512 MiB write) before every step, outside the events"},
         "ms_per_call": {"mean": ms, "median": statistics.median(per), "min": min(per)},
-        "warm_l2_ms_per_call": {"median": statistics.median(warm), "min": min(warm),
-                                "tflops_at_median": flops / (statistics.median(warm) * 1e-3) / 1e12,
-                                "note": "no flush between calls; secondary to the flushed value"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": None,
                      "peak_source": f"{src}: copy bandwidth", "kernel": "quantize_rows + append_kv"},

@@ -124,13 +124,28 @@ struct AppendParams {
   int k_per_token, v_per_head, kv_nhd;
 };
 
-// One warp per new token: lane 0 finds the token's sequence and page once, then the two
-// half-warps take two heads at a time, each with its K and V rows in flight together.
+// One warp per new token.  The token's first four heads of K and V are loaded before its
+// page is looked up, so that the lookup's dependent reads (the sequence by binary search over
+// cu_new, then the block table) overlap those loads; the two half-warps then take two heads at
+// a time, four heads per batch of loads (deeper batches cost occupancy and measured slower).
+constexpr int APPEND_PAIRS = 2;  // head pairs loaded per batch
+
 __global__ void __launch_bounds__(THREADS) append_kv_kernel(const AppendParams p) {
   const int lane = threadIdx.x & 31, hl = lane & 15, hw = lane >> 4;
   const int warps = gridDim.x * (THREADS / 32);
   for (int tok = blockIdx.x * (THREADS / 32) + (threadIdx.x >> 5); tok < p.total_new;
        tok += warps) {
+    uint4 wk[APPEND_PAIRS], wv[APPEND_PAIRS];
+    auto load = [&](int g0) {
+#pragma unroll
+      for (int j = 0; j < APPEND_PAIRS; ++j) {
+        const int g = g0 + 2 * j + hw;
+        const long long r = (long long)tok * p.N2 + g;
+        wk[j] = g < p.N2 ? p.k_new[r * 16 + hl] : make_uint4(0, 0, 0, 0);
+        wv[j] = g < p.N2 ? p.v_new[r * 16 + hl] : make_uint4(0, 0, 0, 0);
+      }
+    };
+    load(0);
     long long slot = 0;
     int pg = -1;
     if (lane == 0) {
@@ -153,24 +168,25 @@ __global__ void __launch_bounds__(THREADS) append_kv_kernel(const AppendParams p
     pg = __shfl_sync(0xffffffffu, pg, 0);
     slot = __shfl_sync(0xffffffffu, slot, 0);
     if (pg < 0) continue;  // warp-uniform
-    for (int g0 = 0; g0 < p.N2; g0 += 2) {
-      const int g = g0 + hw;
-      const bool live = g < p.N2;
-      const long long r = (long long)tok * p.N2 + g;
-      const long long dst = ((long long)pg * p.N2 + g) * p.ps + slot;  // K descale index
-      const long long row = p.kv_nhd ? ((long long)pg * p.ps + slot) * p.N2 + g : dst;
-      const uint4 wk = live ? p.k_new[r * 16 + hl] : make_uint4(0, 0, 0, 0);
-      const uint4 wv = live ? p.v_new[r * 16 + hl] : make_uint4(0, 0, 0, 0);
-      float v[8];
-      unpack8(wk, v);
-      // the shuffles of row_amax run on every lane, live or not
-      const float amax = row_amax(v);
-      if (live) {
-        const float d = p.k_per_token ? descale_of(amax) : p.k_scale[0];
-        p.k_pages[row * 16 + hl] = codes8(v, d);
-        if (p.k_per_token && hl == 0) p.k_descale[dst] = d;
-        unpack8(wv, v);
-        p.v_pages[row * 16 + hl] = codes8(v, p.v_per_head ? p.v_scale[g] : p.v_scale[0]);
+    for (int g0 = 0; g0 < p.N2; g0 += 2 * APPEND_PAIRS) {
+      if (g0 > 0) load(g0);
+#pragma unroll
+      for (int j = 0; j < APPEND_PAIRS; ++j) {
+        const int g = g0 + 2 * j + hw;
+        const bool live = g < p.N2;
+        const long long dst = ((long long)pg * p.N2 + g) * p.ps + slot;  // K descale index
+        const long long row = p.kv_nhd ? ((long long)pg * p.ps + slot) * p.N2 + g : dst;
+        float v[8];
+        unpack8(wk[j], v);
+        // the shuffles of row_amax run on every lane, live or not
+        const float amax = row_amax(v);
+        if (live) {
+          const float d = p.k_per_token ? descale_of(amax) : p.k_scale[0];
+          p.k_pages[row * 16 + hl] = codes8(v, d);
+          if (p.k_per_token && hl == 0) p.k_descale[dst] = d;
+          unpack8(wv[j], v);
+          p.v_pages[row * 16 + hl] = codes8(v, p.v_per_head ? p.v_scale[g] : p.v_scale[0]);
+        }
       }
     }
   }
