@@ -534,6 +534,12 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
     const float rs_abs = fmaxf(fabsf(row_scale), 1e-30f);
     const uint64_t rs2 = ptx::pk(rs_abs, rs_abs);
     float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum (same m in both)
+    // S is read with tcgen05.ld.red, which also returns the largest value the thread loaded.
+    // With a per-tensor K descale and no negative row scale the logits are S times a positive
+    // factor, so on tiles without hidden keys that maximum is the row-half maximum and the
+    // max over the 64 values is skipped; a per-token K descale changes the order, so there
+    // the maximum is taken after the multiply as before.
+    const bool load_max = !p.k_per_token && !any_neg;
     bool ok = true;
     for (int t = 0; t < n; ++t) {
       const uint32_t gt = g + t;
@@ -543,7 +549,9 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
       }
       ptx::tc_fence_after();
       uint32_t x[2][32];
-      ptx::tmem_ld16x2_64<64>(tS, x[0], x[1]);
+      const bool red_tile = load_max && t < t_hidden;
+      float mx_load;
+      ptx::tmem_ld16x2_64_max<64>(tS, x[0], x[1], mx_load);
       ptx::tmem_ld_wait(x[0]);
       ptx::reg_fence(x[1]);
       ptx::tc_fence_before();
@@ -596,15 +604,18 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
               if (c * 32 + j >= lim) x[c][j] = f2u(-INFINITY);
         }
       }
-      float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+      float mx = mx_load;
+      if (!red_tile) {
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        a0 = ptx::max3(a0, u2f(x[0][j]), u2f(x[0][j + 1]));
-        a1 = ptx::max3(a1, u2f(x[0][j + 2]), u2f(x[0][j + 3]));
-        a2 = ptx::max3(a2, u2f(x[1][j]), u2f(x[1][j + 1]));
-        a3 = ptx::max3(a3, u2f(x[1][j + 2]), u2f(x[1][j + 3]));
+        for (int j = 0; j < 32; j += 4) {
+          a0 = ptx::max3(a0, u2f(x[0][j]), u2f(x[0][j + 1]));
+          a1 = ptx::max3(a1, u2f(x[0][j + 2]), u2f(x[0][j + 3]));
+          a2 = ptx::max3(a2, u2f(x[1][j]), u2f(x[1][j + 1]));
+          a3 = ptx::max3(a3, u2f(x[1][j + 2]), u2f(x[1][j + 3]));
+        }
+        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
       }
-      float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the row's other half
       // largest scaled logit of the tile so far (log2 units); -inf while every key is hidden
       const float m_new = fmaxf(m, mx * rs_abs);
