@@ -143,16 +143,8 @@ def cpu_info():
     return oracle.cpu_model(), os.cpu_count()
 
 
-def cpu_baseline(case, lists, counts, seconds, seed=11):
-    """The oracle (exact fp64 mode, all host threads) on a bounded sample of whole tasks."""
-    import oracle
-
-    orc = oracle.Oracle(case)
-    threads = orc.lib.oracle_max_threads()
-    tasks = [(b, h, qt) for b in range(case.B) for h in range(case.N1)
-             for qt in range(-(-case.q_lens[b] // 128))]
-    rng = np.random.default_rng(seed)
-    order = rng.permutation(len(tasks))
+def _oracle_sample(orc, case, lists, counts, tasks, order, mode, seconds):
+    """Times `mode` of the oracle on whole tasks taken in `order` until `seconds` have run."""
     done_flops, done_tasks, done_rows, t_total = 0, 0, 0, 0.0
     i = 0
     while t_total < seconds and i < len(order):
@@ -166,17 +158,36 @@ def cpu_baseline(case, lists, counts, seconds, seed=11):
             ts = lists[b, h, qt, :counts[b, h, qt]].astype(np.int64)
             fl += 4 * 128 * nr * int(np.minimum(128, kl - ts * 128).sum())
         t0 = time.perf_counter()
-        orc.rows(np.array(rows, dtype=np.int32), oracle.EXACT)
+        orc.rows(np.array(rows, dtype=np.int32), mode)
         t_total += time.perf_counter() - t0
         done_flops += fl
         done_tasks += len(chunk)
         done_rows += len(rows)
+    return done_flops, done_tasks, done_rows, t_total
+
+
+def cpu_baseline(case, lists, counts, seconds, seed=11):
+    """The oracle (exact fp64 mode, all host threads) on a bounded sample of whole tasks; its
+    P-emulating mode is timed beside it on a quarter of the time budget."""
+    import oracle
+
+    orc = oracle.Oracle(case)
+    threads = orc.lib.oracle_max_threads()
+    tasks = [(b, h, qt) for b in range(case.B) for h in range(case.N1)
+             for qt in range(-(-case.q_lens[b] // 128))]
+    order = np.random.default_rng(seed).permutation(len(tasks))
+    fl, nt, nr, t = _oracle_sample(orc, case, lists, counts, tasks, order, oracle.EXACT, seconds)
+    pfl, pnt, pnr, pt = _oracle_sample(orc, case, lists, counts, tasks, order, oracle.PEMU,
+                                       seconds / 4)
     model, _ = cpu_info()
-    return {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": threads,
+    return {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"{done_tasks} of {len(tasks)} (b, h, q-tile) tasks ({done_rows} rows), "
-                      f"seeded random, exact fp64 mode, {t_total:.1f} s on {threads} threads "
-                      f"({model})"}
+            "sample": f"{nt} of {len(tasks)} (b, h, q-tile) tasks ({nr} rows), "
+                      f"seeded random, exact fp64 mode, {t:.1f} s on {threads} threads "
+                      f"({model})",
+            "pemu": {"value": pfl / pt / 1e12, "unit": "TFLOP/s",
+                     "sample": f"the first {pnt} of those tasks ({pnr} rows), P-emulating mode, "
+                               f"{pt:.1f} s"}}
 
 
 class ClockSampler:
