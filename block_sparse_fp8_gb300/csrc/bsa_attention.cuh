@@ -13,7 +13,8 @@
 //                   the softmax has read S(t), then O (+)= P(t) V(t).
 //   2 softmax       8 warps; warp (quarter q, sub-block u) owns rows 32q + 16u .. +15 of each
 //   warpgroups      tile, and in it lane i takes row 32q + 16u + i%16 and column half i/16
-//                   (tcgen05.ld shape 16x32bx2), so a row's two halves meet in one shuffle:
+//                   (tcgen05.ld.red shape 16x32bx2, which also returns the thread's maximum
+//                   of the loaded values), so a row's two halves meet in one shuffle:
 //                   scale, the row max, P = 2^(x - m) at the fixed P-scale (exact zeros past the
 //                   causal edge and kv_len) rounded to e4m3 into a 128B-swizzled shared tile
 //                   (the A operand of the PV MMA), O rescaled in TMEM when the row max moves,
@@ -301,7 +302,11 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
     }
   }
   if (lane == 0 && *(volatile int *)&s.abort_flag) {
-    // let the copies still in flight land before shared memory goes away
+    // let the copies still in flight land before shared memory goes away: the last ones of
+    // each ring by their barriers when the loop ended between tasks, and, for copies issued
+    // earlier in an unfinished task, a fixed 20 us settle (a copy lands in a few us)
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 20000) __nanosleep(1000);
     if (qk >= 1) drain_bar(&s.q_full, (qk - 1) & 1);
     for (uint32_t x = g >= KSTAGES ? g - KSTAGES : 0; x < g; ++x) {
       drain_bar(&s.k_full[x % KSTAGES], (x / KSTAGES) & 1);
