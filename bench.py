@@ -143,6 +143,19 @@ def cpu_info():
     return oracle.cpu_model(), os.cpu_count()
 
 
+def _task_rows(case, lists, counts, chunk):
+    """The (token, head) rows of the (b, h, q-tile) tasks in `chunk` and their effective FLOPs
+    (4 * 128 * valid rows * valid keys of every active tile)."""
+    rows, fl = [], 0
+    for b, h, qt in chunk:
+        q0, ql, kl = int(case.cu_seqlens_q[b]), case.q_lens[b], case.kv_lens[b]
+        nr = min(128, ql - qt * 128)
+        rows += [(q0 + qt * 128 + r, h) for r in range(nr)]
+        ts = lists[b, h, qt, :counts[b, h, qt]].astype(np.int64)
+        fl += 4 * 128 * nr * int(np.minimum(128, kl - ts * 128).sum())
+    return np.array(rows, dtype=np.int32).reshape(-1, 2), fl
+
+
 def _oracle_sample(orc, case, lists, counts, tasks, order, mode, seconds):
     """Times `mode` of the oracle on whole tasks taken in `order` until `seconds` have run."""
     done_flops, done_tasks, done_rows, t_total = 0, 0, 0, 0.0
@@ -150,15 +163,9 @@ def _oracle_sample(orc, case, lists, counts, tasks, order, mode, seconds):
     while t_total < seconds and i < len(order):
         chunk = [tasks[j] for j in order[i:i + 8]]
         i += 8
-        rows, fl = [], 0
-        for b, h, qt in chunk:
-            q0, ql, kl = int(case.cu_seqlens_q[b]), case.q_lens[b], case.kv_lens[b]
-            nr = min(128, ql - qt * 128)
-            rows += [(q0 + qt * 128 + r, h) for r in range(nr)]
-            ts = lists[b, h, qt, :counts[b, h, qt]].astype(np.int64)
-            fl += 4 * 128 * nr * int(np.minimum(128, kl - ts * 128).sum())
+        rows, fl = _task_rows(case, lists, counts, chunk)
         t0 = time.perf_counter()
-        orc.rows(np.array(rows, dtype=np.int32), mode)
+        orc.rows(rows, mode)
         t_total += time.perf_counter() - t0
         done_flops += fl
         done_tasks += len(chunk)
@@ -520,16 +527,9 @@ def run_reference(args, rank):
 
     def step(i):
         sel = rng.choice(len(tasks), per_step_tasks, replace=False)
-        rows, fl = [], 0
-        for j in sel:
-            b, h, qt = tasks[j]
-            q0, ql, kl = int(case.cu_seqlens_q[b]), case.q_lens[b], case.kv_lens[b]
-            nr = min(128, ql - qt * 128)
-            rows += [(q0 + qt * 128 + r, h) for r in range(nr)]
-            ts = lists[b, h, qt, :counts[b, h, qt]].astype(np.int64)
-            fl += 4 * 128 * nr * int(np.minimum(128, kl - ts * 128).sum())
+        rows, fl = _task_rows(case, lists, counts, [tasks[j] for j in sel])
         t0 = time.perf_counter()
-        orc.rows(np.array(rows, dtype=np.int32), oracle.EXACT)
+        orc.rows(rows, oracle.EXACT)
         return fl, time.perf_counter() - t0
 
     for i in range(max(args.warmup, 3)):
