@@ -47,7 +47,8 @@ extern "C" {
 typedef enum {
   BSA_OK = 0,
   BSA_ERR_INVALID_ARGUMENT = 1, /* bad dims, scalar, null or misaligned pointer */
-  BSA_ERR_UNSUPPORTED = 2,      /* valid but outside what this build supports (GPU arch, Kb) */
+  BSA_ERR_UNSUPPORTED = 2,      /* valid but outside what this build supports (GPU arch, Kb,
+                                   more than 2^30 (b, h, q-tile) tasks) */
   BSA_ERR_CUDA = 3,             /* a CUDA call or kernel launch failed */
   BSA_ERR_WORKSPACE = 4         /* workspace smaller than bsa_fp8_prefill_workspace_size() */
 } bsa_status_t;
@@ -134,8 +135,8 @@ size_t bsa_fp8_prefill_workspace_size(const bsa_fp8_dims_t *dims);
  *                   At most one of block_mask / sparse_indices; neither = dense path.
  *   softmax_scale   finite (usually 1/sqrt(128))
  *   p_scale         fixed P-scale; <= 0 selects the default 256; must be finite
- *   out_bf16        bf16 [T, N1, 128] (written)
- *   lse_f32         fp32 [N1, T] natural-log LSE (written), or NULL
+ *   out_bf16        bf16 [T, N1, 128] (written), 16-byte aligned
+ *   lse_f32         fp32 [N1, T] natural-log LSE (written), 4-byte aligned; or NULL
  *   workspace       device buffer of at least bsa_fp8_prefill_workspace_size(dims) bytes,
  *                   4-byte aligned (BSA_ERR_WORKSPACE otherwise); overwritten by the call
  *   dev_status      device int, OR-ed with BSA_DEV_* bits on data errors; or NULL
