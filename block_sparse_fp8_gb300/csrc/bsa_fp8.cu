@@ -273,8 +273,85 @@ extern "C" bsa_status_t bsa_fp8_compact_tiles(const bsa_fp8_dims_t *dims, const 
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
-// The prefill; `allow_split` lets it use split-KV when the plan asks for it (the workspace must
-// then hold the plan's bytes).
+// ------------------------------------------------------------------------------------------
+// The workspace of bsa_fp8_prefill_noalloc, for callers that cannot allocate device memory:
+// this file-scope array, 256 bytes on every device that loads the library.
+// ------------------------------------------------------------------------------------------
+
+namespace {
+
+constexpr size_t NOALLOC_SCRATCH_BYTES = 256;
+static_assert(NOALLOC_SCRATCH_BYTES >= WORKSPACE_BYTES,
+              "the array must hold the unsplit prefill's workspace");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+// Host code cannot pass g_noalloc_scratch itself to a kernel (on the host that name is only a
+// stand-in for the device symbol): look up the device address with the device current and
+// reuse it.  The address belongs to the context the module was loaded into, so it is cached
+// together with that context's ID and looked up again when the ID changes (a device reset or
+// a recreated primary context loads the module afresh, possibly at another address).
+struct NoallocAddr {
+  unsigned long long ctx_id = 0;
+  void *ptr = nullptr;
+};
+NoallocAddr g_noalloc_addr[64];
+std::mutex g_noalloc_mu;
+
+struct CtxFns {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+
+const CtxFns &ctx_fns() {
+  static CtxFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
+    ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(ptr);
+  });
+  return fns;
+}
+
+// Called after check_device(), so the device's primary context is current.
+bsa_status_t noalloc_scratch(void **addr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return BSA_ERR_UNSUPPORTED;
+  const CtxFns &fns = ctx_fns();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!fns.get_current || !fns.get_id || fns.get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      fns.get_id(ctx, &id) != CUDA_SUCCESS)
+    return BSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoallocAddr &a = g_noalloc_addr[dev];
+  if (!a.ptr || a.ctx_id != id) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+      (void)cudaGetLastError();  // leave no pending error behind for the caller
+      return BSA_ERR_CUDA;
+    }
+    a.ptr = ptr;
+    a.ctx_id = id;
+  }
+  *addr = a.ptr;
+  return BSA_OK;
+}
+
+}  // namespace
+
+// The prefill.  With `noalloc` it ignores workspace / workspace_bytes and uses the library's
+// own array instead (never split-KV); otherwise the caller's workspace must hold the split
+// plan's bytes.
 static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, const void *k_pages,
                                  const void *v_pages, const float *q_descale,
                                  const float *k_descale, const float *v_descale,
@@ -283,7 +360,7 @@ static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, cons
                                  const int *sparse_indices, const int *sparse_seq_len,
                                  float softmax_scale, float p_scale, void *out_bf16,
                                  float *lse_f32, void *workspace, size_t workspace_bytes,
-                                 int *dev_status, void *stream, bool allow_split) {
+                                 int *dev_status, void *stream, bool noalloc) {
   bsa_status_t st = validate_dims(dims);
   if (st != BSA_OK) return st;
   if (block_mask && sparse_indices) return BSA_ERR_INVALID_ARGUMENT;
@@ -302,14 +379,21 @@ static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, cons
       (p.k_per_token && !aligned16(k_descale)) || !aligned16(out_bf16) ||
       (reinterpret_cast<uintptr_t>(lse_f32) & 3u) != 0)
     return BSA_ERR_INVALID_ARGUMENT;
-  if (!workspace || workspace_bytes < WORKSPACE_BYTES ||
-      (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
+  if (!noalloc && (!workspace || workspace_bytes < WORKSPACE_BYTES ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0))
     return BSA_ERR_WORKSPACE;
   const size_t smem = attn::smem_bytes(p.Kb);
   int num_sms = 0, per_sm = 1;
   st = check_device(smem, &num_sms, &per_sm);
   if (st != BSA_OK) return st;
-  const SplitPlan plan = plan_splits(p, num_sms, allow_split);
+  if (noalloc) {
+    // the library's own array, looked up only once every argument has been checked
+    st = noalloc_scratch(&workspace);
+    if (st != BSA_OK) return st;
+    workspace_bytes = NOALLOC_SCRATCH_BYTES;
+  }
+  // the array-backed entry point never splits: its array holds the item counter only
+  const SplitPlan plan = plan_splits(p, num_sms, !noalloc);
   if (workspace_bytes < plan.bytes ||
       (plan.splits > 1 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
     return BSA_ERR_WORKSPACE;
@@ -392,7 +476,7 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
   return prefill_impl(dims, q, k_pages, v_pages, q_descale, k_descale, v_descale, cu_seqlens_q,
                       seqused_kv, block_table, block_mask, sparse_indices, sparse_seq_len,
                       softmax_scale, p_scale, out_bf16, lse_f32, workspace, workspace_bytes,
-                      dev_status, stream, true);
+                      dev_status, stream, false);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -485,39 +569,6 @@ extern "C" bsa_status_t bsa_fp8_append_kv(const bsa_fp8_append_dims_t *d, const 
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
-// ------------------------------------------------------------------------------------------
-// bsa_fp8_prefill_noalloc: the same prefill for callers that cannot allocate device memory.
-// Its workspace is this file-scope array, 256 bytes on every device that loads the library.
-// ------------------------------------------------------------------------------------------
-
-namespace {
-
-constexpr size_t NOALLOC_SCRATCH_BYTES = 256;
-static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
-
-// Host code cannot pass g_noalloc_scratch itself to a kernel (on the host that name is only a
-// stand-in for the device symbol): look up the device address once per device, with that
-// device current, and reuse it.
-void *g_noalloc_addr[64] = {nullptr};
-std::mutex g_noalloc_mu;
-
-bsa_status_t noalloc_scratch(void **addr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return BSA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
-      return BSA_ERR_CUDA;
-    g_noalloc_addr[dev] = ptr;
-  }
-  *addr = g_noalloc_addr[dev];
-  return BSA_OK;
-}
-
-}  // namespace
-
 extern "C" bsa_status_t bsa_fp8_prefill_noalloc(
     const bsa_fp8_dims_t *dims, const void *q, const void *k_pages, const void *v_pages,
     const float *q_descale, const float *k_descale, const float *v_descale,
@@ -525,13 +576,9 @@ extern "C" bsa_status_t bsa_fp8_prefill_noalloc(
     const uint8_t *block_mask, const int *sparse_indices, const int *sparse_seq_len,
     float softmax_scale, float p_scale, void *out_bf16, float *lse_f32, int *dev_status,
     void *stream) {
-  // the array is a fixed 256 bytes, all the unsplit prefill needs
-  void *scratch = nullptr;
-  const bsa_status_t st = noalloc_scratch(&scratch);
-  if (st != BSA_OK) return st;
-  // the array holds the item counter only: this entry point never splits the KV lists
+  // every argument is checked as bsa_fp8_prefill checks it; the array is looked up after that
   return prefill_impl(dims, q, k_pages, v_pages, q_descale, k_descale, v_descale, cu_seqlens_q,
                       seqused_kv, block_table, block_mask, sparse_indices, sparse_seq_len,
-                      softmax_scale, p_scale, out_bf16, lse_f32, scratch, NOALLOC_SCRATCH_BYTES,
-                      dev_status, stream, false);
+                      softmax_scale, p_scale, out_bf16, lse_f32, nullptr, 0, dev_status, stream,
+                      true);
 }

@@ -181,9 +181,12 @@ bsa_status_t bsa_fp8_compact_tiles(const bsa_fp8_dims_t *dims, const int *cu_seq
  *     `workspace` / `workspace_bytes`.  It never uses split-KV, so every valid problem fits
  *     the 256-byte array; a problem for which bsa_fp8_prefill would split runs unsplit here
  *     (the same result up to the rounding of P against each slice's own running max).
- *   - The first call on a device (with that device current) looks up the array's device
- *     address once; make that first call before any stream capture.  Failure of the lookup
- *     is BSA_ERR_CUDA.
+ *   - Arguments are checked first, exactly as bsa_fp8_prefill checks them.  Then the first
+ *     call on a device (with that device current) looks up the array's device address and
+ *     keeps it for later calls; the address is tied to the device's current context and
+ *     looked up again after a device reset or a new primary context.  Make that first call
+ *     before any stream capture.  A failed lookup returns BSA_ERR_CUDA and leaves no pending
+ *     CUDA error.
  *   - Every call on a device shares the one array, which keeps the previous call's contents
  *     (the call clears what must start at zero on `stream` itself).  Calls whose work
  *     overlaps on the GPU -- on different streams without ordering between them -- race on

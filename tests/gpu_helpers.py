@@ -21,6 +21,18 @@ PEMU_ATOL, PEMU_RTOL = 1e-4, 0.0078125
 LSE_ATOL, LSE_RTOL = 2.5e-5, 0.005
 MAX_OUTSIDE = 0.005
 
+# few (b, h, q-tile) tasks over a long KV: bsa_fp8_prefill cuts each task's active list into
+# slices (split-KV) for these
+SPLIT_CASES = {
+    "split_long_kv": dict(seed=201, q_lens=[256], kv_lens=[8229], N1=2, N2=1, page_size=64,
+                          k_scale_kind=1, v_scale_kind=2, mask="bernoulli", keep=0.5),
+    "split_chunked": dict(seed=202, q_lens=[384], kv_lens=[16384], N1=4, N2=2, page_size=32,
+                          k_scale_kind=1, v_scale_kind=2, mask="local_sink", n_local=2,
+                          p_far=0.3),
+    "split_dense_noncausal": dict(seed=203, q_lens=[130, 70], kv_lens=[9000, 8300], N1=2,
+                                  N2=2, page_size=64, mask="none", causal=0),
+}
+
 
 def ensure_built():
     from block_sparse_fp8_gb300 import _build

@@ -131,3 +131,36 @@ def test_workspace_required(L):
     assert call(None, 0) == 4                 # BSA_ERR_WORKSPACE
     assert call(0x20000, 255) == 4            # too small
     assert call(0x20002, 256) == 4            # misaligned
+
+
+def _noalloc(L, dims, **ptrs):
+    fake = 0x10000  # never dereferenced: every case below fails validation first
+    args = dict(q=fake, k=fake, v=fake, qd=fake, kd=fake, vd=fake, cu=fake, su=fake, bt=fake,
+                mask=None, idx=None, sl=None, scale=0.088, pscale=256.0, out=fake, lse=fake)
+    args.update(ptrs)
+    return L.bsa_fp8_prefill_noalloc(ctypes.byref(dims), args["q"], args["k"], args["v"],
+                                     args["qd"], args["kd"], args["vd"], args["cu"], args["su"],
+                                     args["bt"], args["mask"], args["idx"], args["sl"],
+                                     args["scale"], args["pscale"], args["out"], args["lse"],
+                                     None, None)
+
+
+@pytest.mark.parametrize("bad", [dict(D=64), dict(page_size=48), dict(N1=6, N2=4),
+                                 dict(max_pages_per_seq=15), dict(causal=2)])
+def test_noalloc_validates_like_prefill(L, bad):
+    """The array-backed entry point checks its arguments before it touches the device, so its
+    error codes are those of bsa_fp8_prefill (no GPU is needed to reach them)."""
+    d = _dims(**bad)
+    assert _noalloc(L, d) == _prefill(L, d) == INVALID
+
+
+def test_noalloc_scalar_pointer_and_size_checks(L):
+    d = _dims()
+    assert _noalloc(L, d, scale=float("nan")) == INVALID
+    assert _noalloc(L, d, mask=0x20000, idx=0x30000, sl=0x40000) == INVALID
+    for k in ("q", "k", "v", "qd", "kd", "vd", "cu", "bt", "out"):
+        assert _noalloc(L, d, **{k: None}) == INVALID, k
+    assert _noalloc(L, d, q=0x10001) == INVALID
+    assert _noalloc(L, _dims(max_kv_len=4097 * 128, max_pages_per_seq=4097 * 2,
+                             num_pages=8194)) == UNSUPPORTED
+    assert _noalloc(L, _dims(B=0, total_q=0)) == 0

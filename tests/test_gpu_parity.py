@@ -7,8 +7,9 @@ import torch
 
 import oracle as O
 import workloads as W
-from gpu_helpers import (EXACT_ATOL, EXACT_RTOL, NEG_FLT_MAX, PEMU_ATOL, PEMU_RTOL, check_lse,
-                         check_o, ensure_built, run, run_lists, sample_rows, to_device)
+from gpu_helpers import (EXACT_ATOL, EXACT_RTOL, NEG_FLT_MAX, PEMU_ATOL, PEMU_RTOL, SPLIT_CASES,
+                         check_lse, check_o, ensure_built, run, run_lists, sample_rows,
+                         to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -336,15 +337,6 @@ def _expected_splits(case, num_sms):
     return max(1, min(8, pipes // ntasks, case.Kb // 16))
 
 
-SPLIT_CASES = {
-    "split_long_kv": dict(seed=201, q_lens=[256], kv_lens=[8229], N1=2, N2=1, page_size=64,
-                          k_scale_kind=1, v_scale_kind=2, mask="bernoulli", keep=0.5),
-    "split_chunked": dict(seed=202, q_lens=[384], kv_lens=[16384], N1=4, N2=2, page_size=32,
-                          k_scale_kind=1, v_scale_kind=2, mask="local_sink", n_local=2,
-                          p_far=0.3),
-    "split_dense_noncausal": dict(seed=203, q_lens=[130, 70], kv_lens=[9000, 8300], N1=2,
-                                  N2=2, page_size=64, mask="none", causal=0),
-}
 
 
 @pytest.mark.parametrize("name", sorted(SPLIT_CASES))
