@@ -8,7 +8,8 @@
 //                   publishes the task, then streams Q and, tile by tile, the K pages, the
 //                   per-token K descales and the V pages through TMA (2-stage rings; masked
 //                   tiles are never addressed; a missing page is read at an out-of-range
-//                   coordinate, which fills zeros).
+//                   coordinate, which fills zeros).  The whole warp looks up the physical
+//                   pages of 32 list tiles at once, a batch ahead of lane 0's copies.
 //   MMA warp        one thread issues tcgen05.mma kind::f8f6f4: S(t+1) = Q K(t+1)^T as soon as
 //                   the softmax has read S(t), then O (+)= P(t) V(t).
 //   2 softmax       8 warps; warp (quarter q, sub-block u) owns rows 32q + 16u .. +15 of each
@@ -72,6 +73,7 @@ struct __align__(1024) Pipe {
   float kd[KDSTAGES][KD_STRIDE];
   TaskInfo info[2];
   uint32_t bitmap[KB_MAX / 32];
+  int pg[2][32][4];  // physical pages of 32 consecutive list tiles, two batches (producer)
   uint64_t task_full[2], task_empty[2];
   uint64_t q_full, q_empty;
   uint64_t k_full[KSTAGES], k_empty[KSTAGES];
@@ -220,70 +222,98 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
       ptx::mbar_arrive(&s.task_full[slot]);
     }
     ++k;
-    if (lane == 0 && n > 0) {
+    if (n > 0) {
       const int g_kv = h / p.G;
-      if (qk >= 1 && !wait_bar(p, s, &s.q_empty, (qk - 1) & 1)) ok = false;
-      if (ok) {
-        ptx::mbar_arrive_expect_tx(&s.q_full, TILE * HEAD_DIM);
-        const int tok0 = geo.q0 + qt * TILE;  // the Q box is 128 tokens of head h either way
-        ptx::tma_load_3d(s.q, tmap_q, &s.q_full, 0, p.q_ntd ? tok0 : h, p.q_ntd ? h : tok0);
+      // The physical pages of list tiles lo + 32 j .. + 31 are looked up by the whole warp at
+      // once (lane i: tile 32 j + i), one batch ahead of their use, so that the dependent
+      // block_table loads do not sit between consecutive tiles' copies.
+      int pf[4];
+      auto lookup = [&](int t0) {
+        const int t = t0 + lane;
+        if (t < n) {
+          tile_pages(p, b, list[lo + t], geo.kv_len, pf);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) pf[i] = p.num_pages;
+        }
+      };
+      lookup(0);
+      if (lane == 0) {
+        if (qk >= 1 && !wait_bar(p, s, &s.q_empty, (qk - 1) & 1)) ok = false;
+        if (ok) {
+          ptx::mbar_arrive_expect_tx(&s.q_full, TILE * HEAD_DIM);
+          const int tok0 = geo.q0 + qt * TILE;  // the Q box is 128 tokens of head h either way
+          ptx::tma_load_3d(s.q, tmap_q, &s.q_full, 0, p.q_ntd ? tok0 : h, p.q_ntd ? h : tok0);
+        }
       }
       ++qk;
       int prev[4] = {0, 0, 0, 0};
-      for (int t = 0; ok && t <= n; ++t) {
-        int pgs[4] = {0, 0, 0, 0};
-        if (t < n) {
-          const int tile = list[lo + t];
-          const int nvalid = tile_pages(p, b, tile, geo.kv_len, pgs);
-          const uint32_t gk = g + t;
-          const int ks = gk % KSTAGES;
-          if (gk >= KSTAGES && !wait_bar(p, s, &s.k_empty[ks], ((gk / KSTAGES) - 1) & 1)) {
-            ok = false;
-            break;
-          }
-          ptx::mbar_arrive_expect_tx(&s.k_full[ks], TILE * HEAD_DIM);
+      for (int t = 0; t <= n; ++t) {
+        if ((t & 31) == 0 && t < n) {
+          // batch t / 32 becomes current; start the next one
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (i < npg)
-              ptx::tma_load_4d(s.k[ks] + i * p.ps * HEAD_DIM, tmap_k, &s.k_full[ks], 0,
-                               p.kv_nhd ? g_kv : 0, p.kv_nhd ? 0 : g_kv, pgs[i]);
-          if (p.k_per_token) {
-            const int ds = gk % KDSTAGES;
-            if (gk >= KDSTAGES && !wait_bar(p, s, &s.kd_empty[ds], ((gk / KDSTAGES) - 1) & 1)) {
+          for (int i = 0; i < 4; ++i) s.pg[(t >> 5) & 1][lane][i] = pf[i];
+          __syncwarp();
+          if (t + 32 < n) lookup(t + 32);
+        }
+        if (lane == 0 && ok) {
+          int pgs[4] = {0, 0, 0, 0};
+          if (t < n) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pgs[i] = s.pg[(t >> 5) & 1][t & 31][i];
+            const uint32_t gk = g + t;
+            const int ks = gk % KSTAGES;
+            if (gk >= KSTAGES && !wait_bar(p, s, &s.k_empty[ks], ((gk / KSTAGES) - 1) & 1)) {
               ok = false;
-              break;
+            } else {
+              ptx::mbar_arrive_expect_tx(&s.k_full[ks], TILE * HEAD_DIM);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (i < npg)
+                  ptx::tma_load_4d(s.k[ks] + i * p.ps * HEAD_DIM, tmap_k, &s.k_full[ks], 0,
+                                   p.kv_nhd ? g_kv : 0, p.kv_nhd ? 0 : g_kv, pgs[i]);
+              if (p.k_per_token) {
+                const int ds = gk % KDSTAGES;
+                if (gk >= KDSTAGES &&
+                    !wait_bar(p, s, &s.kd_empty[ds], ((gk / KDSTAGES) - 1) & 1)) {
+                  ok = false;
+                } else {
+                  int nvalid = 0;
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) nvalid += (i < npg && pgs[i] < p.num_pages);
+                  ptx::mbar_arrive_expect_tx(&s.kd_full[ds], (uint32_t)(nvalid * p.ps * 4));
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    if (i < npg && pgs[i] < p.num_pages)
+                      ptx::bulk_load(&s.kd[ds][kd_index(i * p.ps)],
+                                     p.k_descale + ((size_t)pgs[i] * p.N2 + g_kv) * p.ps,
+                                     (uint32_t)(p.ps * 4), &s.kd_full[ds]);
+                }
+              }
             }
-            ptx::mbar_arrive_expect_tx(&s.kd_full[ds], (uint32_t)(nvalid * p.ps * 4));
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              if (i < npg && pgs[i] < p.num_pages)
-                ptx::bulk_load(&s.kd[ds][kd_index(i * p.ps)],
-                               p.k_descale + ((size_t)pgs[i] * p.N2 + g_kv) * p.ps,
-                               (uint32_t)(p.ps * 4), &s.kd_full[ds]);
           }
-        }
-        if (t >= 1) {
-          // V of the previous tile: K runs one tile ahead of V, in the order the MMAs consume
-          // them (S(t) is issued before PV(t-1))
-          const uint32_t gv = g + t - 1;
-          const int vs = gv % VSTAGES;
-          if (gv >= VSTAGES && !wait_bar(p, s, &s.v_empty[vs], ((gv / VSTAGES) - 1) & 1)) {
-            ok = false;
-            break;
-          }
-          ptx::mbar_arrive_expect_tx(&s.v_full[vs], TILE * HEAD_DIM);
+          if (ok && t >= 1) {
+            // V of the previous tile: K runs one tile ahead of V, in the order the MMAs
+            // consume them (S(t) is issued before PV(t-1))
+            const uint32_t gv = g + t - 1;
+            const int vs = gv % VSTAGES;
+            if (gv >= VSTAGES && !wait_bar(p, s, &s.v_empty[vs], ((gv / VSTAGES) - 1) & 1)) {
+              ok = false;
+            } else {
+              ptx::mbar_arrive_expect_tx(&s.v_full[vs], TILE * HEAD_DIM);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (i < npg)
-              ptx::tma_load_4d(s.v[vs] + i * p.ps * HEAD_DIM, tmap_v, &s.v_full[vs], 0,
-                               p.kv_nhd ? g_kv : 0, p.kv_nhd ? 0 : g_kv, prev[i]);
-        }
-        if (t < n) {
+              for (int i = 0; i < 4; ++i)
+                if (i < npg)
+                  ptx::tma_load_4d(s.v[vs] + i * p.ps * HEAD_DIM, tmap_v, &s.v_full[vs], 0,
+                                   p.kv_nhd ? g_kv : 0, p.kv_nhd ? 0 : g_kv, prev[i]);
+            }
+          }
 #pragma unroll
           for (int i = 0; i < 4; ++i) prev[i] = pgs[i];
         }
+        if ((t & 31) == 31 && !__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       }
-      g += n;
+      if (ok) g += n;  // lane 0's count is the one broadcast below
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     g = __shfl_sync(0xffffffffu, g, 0);
