@@ -3,9 +3,12 @@
 
 One step = one bsa_fp8_prefill call over the whole workload (active-tile compaction, paged
 TMA loads, tcgen05 QK^T and PV, online softmax with e4m3 P, epilogue), inputs resident in HBM.
-The default workload is 2 x 8192-token prefills, 32 query / 8 KV heads, page 64, per-token K
-and per-head V descales, 1% outlier channels, block mask keeping each causal off-diagonal tile
-with probability 0.5 (the diagonal always kept).
+The default workload is the largest block-sparse one: a varlen batch of four prefills of
+16384, 12000, 9000 and 4097 tokens, 64 query / 8 KV heads, page 32, per-token K and per-head V
+descales, sparse index lists holding 25% of each Q tile's causal KV tiles (tile 0 and the
+diagonal always in), two empty tasks.  The same JSON line reports the other full-size
+workloads (2 x 8K block mask, 4K over a 64K cache, dense 32K), timed the same way, under
+"other_workloads".
 
 Metric: effective TFLOP/s over active tiles, FLOPs = sum over (task, active tile) of
 4 * 128 * rows_valid * cols_valid.  Prints one JSON line (rank 0).
@@ -36,7 +39,9 @@ import workloads as W  # noqa: E402
 
 METRIC = ("block-sparse FP8 prefill effective TFLOPS (active tiles) and ms/call, "
           "% FP8 roofline")
-DEFAULT_WORKLOAD = "prefill_2x8k_h32kv8_bsm50_outliers"
+DEFAULT_WORKLOAD = "varlen_4x16k_h64kv8_idx25"
+OTHER_WORKLOADS = ("prefill_2x8k_h32kv8_bsm50_outliers", "chunked_4k_over_64k_h32kv4_local_sink",
+                   "dense_32k_h32kv8")
 FP8_PER_BF16 = 2.0        # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
@@ -52,6 +57,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the other full-size workloads (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--op", choices=["prefill", "quantize"], default="prefill",
                     help="prefill (the hot path, default) or the quantise step that feeds it: "
@@ -262,6 +269,78 @@ def make_workload(args):
         kw["q_lens"] = kw["q_lens"][:args.batch]
         kw["kv_lens"] = kw["kv_lens"][:args.batch]
     return W.make_case(args.workload, **kw)
+
+
+def upload(case, dev):
+    import torch
+
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    return dict(q=t(case.q), k_pages=t(case.k_pages), v_pages=t(case.v_pages),
+                q_descale=t(case.q_descale), k_descale=t(case.k_descale),
+                v_descale=t(case.v_descale), cu_seqlens_q=t(case.cu_seqlens_q),
+                seqused_kv=t(case.seqused_kv), block_table=t(case.block_table),
+                block_mask=t(case.block_mask), sparse_indices=t(case.sparse_indices),
+                sparse_seq_len=t(case.sparse_seq_len))
+
+
+def time_other_workload(name, steps, warmup, dev, flush, fp8_peak, traffic_of):
+    """One more full-size workload timed like the main one (L2 flushed before every step,
+    CUDA events around each call); its buffers are freed before returning."""
+    import torch
+
+    import block_sparse_fp8_gb300 as bsa
+
+    case = W.make_workload(name)
+    d = upload(case, dev)
+    dims = bsa.Dims(**case.dims())
+    lists, counts = bsa.compact_tiles(d["cu_seqlens_q"], d["seqused_kv"], dims,
+                                      block_mask=d["block_mask"],
+                                      sparse_indices=d["sparse_indices"],
+                                      sparse_seq_len=d["sparse_seq_len"])
+    tiles, flops = W.active_work(case, (lists.cpu().numpy(), counts.cpu().numpy()))
+    out = torch.empty((case.T, case.N1, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((case.N1, case.T), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    workspace = torch.empty(max(bsa.workspace_size(dims), 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        bsa.prefill(d["q"], d["k_pages"], d["v_pages"], d["q_descale"], d["k_descale"],
+                    d["v_descale"], d["cu_seqlens_q"], d["seqused_kv"], d["block_table"],
+                    case.max_q_len, case.max_kv_len, block_mask=d["block_mask"],
+                    sparse_indices=d["sparse_indices"], sparse_seq_len=d["sparse_seq_len"],
+                    softmax_scale=case.softmax_scale, p_scale=case.p_scale,
+                    causal=bool(case.causal), out=out, lse=lse, dev_status=status,
+                    workspace=workspace, stream=stream, k_scale_kind=case.k_scale_kind,
+                    v_scale_kind=case.v_scale_kind)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    per = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        per.append(e0.elapsed_time(e1))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"{name}: device status {int(status.item())}")
+    ms = statistics.mean(per)
+    achieved = flops / (ms * 1e-3) / 1e12
+    res = {"ms_per_call": {"mean": ms, "median": statistics.median(per), "min": min(per)},
+           "value": achieved, "unit": "TFLOP/s",
+           "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak,
+                        "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+                        "traffic": traffic_of(name)},
+           "config": config_of(case, name, tiles, flops)}
+    if "fa_convention_gflop" in res["config"]:
+        res["fa_convention_tflops"] = res["config"]["fa_convention_gflop"] * 1e9 / (ms * 1e-3) / 1e12
+    del d, out, lse, workspace
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args, rank, world):
@@ -506,6 +585,16 @@ def run_ours(args, rank, world):
                                         / 1e12)
     if not args.no_cpu_baseline and world >= 1:
         line["cpu_baseline"] = cpu_baseline(case, lists, counts, args.cpu_seconds)
+    if not args.no_others and args.batch == 0:
+        # the other full-size workloads, one after the other on this GPU (not part of the
+        # timed region above)
+        del d, out, lse
+        torch.cuda.empty_cache()
+        steps = max(5, min(args.steps, 20))
+        line["other_workloads"] = {
+            name: time_other_workload(name, steps, max(args.warmup, 3), dev, flush, fp8_peak,
+                                      measured_traffic)
+            for name in OTHER_WORKLOADS if name != args.workload}
     return line
 
 

@@ -49,6 +49,13 @@ def test_prefill_line():
     assert e["host_link"]["h2d_gbs"] > 0 and e["host_link"]["d2h_gbs"] > 0
     assert d["warm_l2_ms_per_call"]["median"] > 0
     assert "sm_mhz" in d["clocks"]
+    # the other full-size workloads, timed the same way, in the same line
+    import bench
+
+    assert set(d["other_workloads"]) == set(bench.OTHER_WORKLOADS)
+    for name, o in d["other_workloads"].items():
+        assert o["config"]["workload"] == name and o["value"] > 0
+        assert o["roofline"]["frac"] == pytest.approx(o["value"] / o["roofline"]["peak"])
 
 
 @pytest.mark.gpu

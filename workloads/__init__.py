@@ -19,6 +19,7 @@ Workload shapes follow the two pages this library implements:
 from __future__ import annotations
 
 import math
+import os
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -60,14 +61,28 @@ def rand_uniform(seed: int, stream: int, n: int, start: int = 0) -> np.ndarray:
     return (u.astype(np.float64) + 0.5) * (1.0 / 9007199254740992.0)
 
 
-def rand_normal(seed: int, stream: int, n: int, chunk: int = 1 << 22) -> np.ndarray:
-    """N(0, 1) as float32 (Box-Muller cosine branch over draw pairs), generated in chunks."""
+def rand_normal(seed: int, stream: int, n: int, chunk: int = 1 << 20) -> np.ndarray:
+    """N(0, 1) as float32 (Box-Muller cosine branch over draw pairs), generated in chunks.
+    The generator is counter-based, so chunks are independent: they run on a thread pool
+    (numpy releases the GIL in these array operations) and the result does not depend on
+    the number of threads."""
+    from concurrent.futures import ThreadPoolExecutor
+
     out = np.empty(n, dtype=np.float32)
-    for s in range(0, n, chunk):
+
+    def fill(s):
         m = min(chunk, n - s)
         u = rand_uniform(seed, stream, 2 * m, start=2 * s)
         u1, u2 = u[0::2], u[1::2]
         out[s:s + m] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+
+    starts = list(range(0, n, chunk))
+    if len(starts) <= 1:
+        for s in starts:
+            fill(s)
+    else:
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1, len(starts))) as ex:
+            list(ex.map(fill, starts))
     return out
 
 
