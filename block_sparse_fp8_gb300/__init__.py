@@ -16,7 +16,7 @@ import os
 from . import _build
 
 __all__ = ["Dims", "AppendDims", "Q_TND", "Q_NTD", "KV_HND", "KV_NHD", "prefill", "compact_tiles", "quantize_rows", "append_kv",
-           "workspace_size", "status_string", "lib",
+           "workspace_size", "status_string", "set_wait_limit_ns", "lib",
            "SCALE_PER_TENSOR", "SCALE_PER_TOKEN_HEAD", "SCALE_PER_HEAD", "BsaError",
            "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_BAD_SEQLEN", "DEV_TIMEOUT"]
 
@@ -31,7 +31,7 @@ DEV_TIMEOUT = 8
 
 EXPORTED = ("bsa_fp8_prefill", "bsa_fp8_prefill_workspace_size", "bsa_fp8_compact_tiles",
             "bsa_fp8_prefill_noalloc", "bsa_fp8_quantize_rows", "bsa_fp8_append_kv",
-            "bsa_status_string")
+            "bsa_fp8_set_wait_limit_ns", "bsa_status_string")
 
 
 class BsaError(RuntimeError):
@@ -83,10 +83,18 @@ def lib():
         L.bsa_fp8_quantize_rows.argtypes = [vp, ctypes.c_longlong, vp, vp, vp]
         L.bsa_fp8_append_kv.restype = i32
         L.bsa_fp8_append_kv.argtypes = [ctypes.POINTER(AppendDims)] + [vp] * 12
+        L.bsa_fp8_set_wait_limit_ns.restype = i32
+        L.bsa_fp8_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         L.bsa_status_string.restype = ctypes.c_char_p
         L.bsa_status_string.argtypes = [i32]
         _lib = L
     return _lib
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of every bounded wait inside the prefill kernel for later launches (0: the
+    default, 2 s).  A wait that runs out sets DEV_TIMEOUT in the device status word."""
+    lib().bsa_fp8_set_wait_limit_ns(int(ns))
 
 
 def status_string(status: int) -> str:

@@ -103,11 +103,13 @@ __device__ __forceinline__ bool wait_bar(const Params &p, Pipe &s, uint64_t *bar
                                          uint32_t parity) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
+  // a probe suspends the thread for at most the launch's limit, so that a short limit holds
+  const uint32_t hint = (uint32_t)min(p.wait_limit_ns, (unsigned long long)WAIT_LIMIT_NS);
   for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
+    if (ptx::mbar_try_wait_hint(bar, parity, hint)) return true;
+    if ((it & 63u) == 1) {  // the first failed probe, then every 64th
       if (*(volatile int *)&s.abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      if (ptx::globaltimer_ns() - t0 > p.wait_limit_ns) {
         report(p, BSA_DEV_TIMEOUT);
         *(volatile int *)&s.abort_flag = 1;
         return false;
@@ -130,7 +132,8 @@ __device__ __forceinline__ bool wait_bar_warp(const Params &p, Pipe &s, uint64_t
   return wait_bar_warp_slow(p, s, bar, parity);
 }
 
-// Bounded wait that ignores the abort flag (used to let in-flight async work land).
+// Bounded wait that ignores the abort flag and the launch's wait limit (used to let in-flight
+// async work land before the CTA exits).
 __device__ __forceinline__ void drain_bar(uint64_t *bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer_ns();
   while (!ptx::mbar_try_wait(bar, parity)) {
@@ -176,6 +179,10 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
   int k = 0, qk = 0;
   uint32_t g = 0;
   bool ok = true;
+  // Copies issued into each ring (lane 0): qk Q tiles; K, K-descale and V tiles for the g
+  // finished tiles, or -- recorded only where a wait fails in the middle of a task -- fk >> 1 K
+  // tiles (one descale tile fewer if fk & 1) and fv V tiles.
+  uint32_t fk = ~0u, fv = 0;
   for (;;) {
     // claim the next work item: items are numbered by Q tile, descending, so the longest
     // causal tasks go first and a pipeline that finishes early takes the next one
@@ -244,9 +251,9 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
           ptx::mbar_arrive_expect_tx(&s.q_full, TILE * HEAD_DIM);
           const int tok0 = geo.q0 + qt * TILE;  // the Q box is 128 tokens of head h either way
           ptx::tma_load_3d(s.q, tmap_q, &s.q_full, 0, p.q_ntd ? tok0 : h, p.q_ntd ? h : tok0);
+          ++qk;  // lane 0 counts the Q copies issued; the others take its count below
         }
       }
-      ++qk;
       int prev[4] = {0, 0, 0, 0};
       for (int t = 0; t <= n; ++t) {
         if ((t & 31) == 0 && t < n) {
@@ -264,7 +271,9 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
             const uint32_t gk = g + t;
             const int ks = gk % KSTAGES;
             if (gk >= KSTAGES && !wait_bar(p, s, &s.k_empty[ks], ((gk / KSTAGES) - 1) & 1)) {
-              ok = false;
+              ok = false;  // K, descales and V issued for tiles < t, < t, < t - 1
+              fk = gk << 1;
+              fv = t >= 1 ? gk - 1 : g;
             } else {
               ptx::mbar_arrive_expect_tx(&s.k_full[ks], TILE * HEAD_DIM);
 #pragma unroll
@@ -276,7 +285,9 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
                 const int ds = gk % KDSTAGES;
                 if (gk >= KDSTAGES &&
                     !wait_bar(p, s, &s.kd_empty[ds], ((gk / KDSTAGES) - 1) & 1)) {
-                  ok = false;
+                  ok = false;  // K issued for tile t too, its descales not
+                  fk = ((gk + 1) << 1) | 1u;
+                  fv = t >= 1 ? gk - 1 : g;
                 } else {
                   int nvalid = 0;
 #pragma unroll
@@ -298,7 +309,9 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
             const uint32_t gv = g + t - 1;
             const int vs = gv % VSTAGES;
             if (gv >= VSTAGES && !wait_bar(p, s, &s.v_empty[vs], ((gv / VSTAGES) - 1) & 1)) {
-              ok = false;
+              ok = false;  // K and descales issued for tiles <= t (the list has n), V for < t - 1
+              fk = (g + min(t + 1, n)) << 1;
+              fv = gv;
             } else {
               ptx::mbar_arrive_expect_tx(&s.v_full[vs], TILE * HEAD_DIM);
 #pragma unroll
@@ -332,17 +345,19 @@ __device__ __forceinline__ void run_producer(const Params &p, Pipe &s, uint16_t 
     }
   }
   if (lane == 0 && *(volatile int *)&s.abort_flag) {
-    // let the copies still in flight land before shared memory goes away: the last ones of
-    // each ring by their barriers when the loop ended between tasks, and, for copies issued
-    // earlier in an unfinished task, a fixed 20 us settle (a copy lands in a few us)
-    const uint64_t t0 = ptx::globaltimer_ns();
-    while (ptx::globaltimer_ns() - t0 < 20000) __nanosleep(1000);
+    // every copy issued must land before shared memory goes away: the last copy issued into
+    // each slot of each ring completes its slot's latest phase, and a slot's phases complete
+    // in order, so waiting for those phases covers every earlier copy too
+    const bool mid = fk != ~0u;
+    const uint32_t nk = mid ? fk >> 1 : g, nkd = nk - (mid ? (fk & 1u) : 0u), nv = mid ? fv : g;
+    auto drain_ring = [&](uint64_t *full, uint32_t stages, uint32_t issued) {
+      for (uint32_t x = issued >= stages ? issued - stages : 0; x < issued; ++x)
+        drain_bar(&full[x % stages], (x / stages) & 1);
+    };
     if (qk >= 1) drain_bar(&s.q_full, (qk - 1) & 1);
-    for (uint32_t x = g >= KSTAGES ? g - KSTAGES : 0; x < g; ++x) {
-      drain_bar(&s.k_full[x % KSTAGES], (x / KSTAGES) & 1);
-      drain_bar(&s.v_full[x % VSTAGES], (x / VSTAGES) & 1);
-      if (p.k_per_token) drain_bar(&s.kd_full[x % KDSTAGES], (x / KDSTAGES) & 1);
-    }
+    drain_ring(s.k_full, KSTAGES, nk);
+    drain_ring(s.v_full, VSTAGES, nv);
+    if (p.k_per_token) drain_ring(s.kd_full, KDSTAGES, nkd);
   }
 }
 

@@ -13,7 +13,10 @@ namespace bsa {
 constexpr int TILE = 128;
 constexpr int HEAD_DIM = 128;
 constexpr int KB_MAX = 4096;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: far above any legitimate wait
+// Default limit of a bounded wait inside the kernels (2 s: far above any legitimate wait); the
+// host may lower it for a launch (Params::wait_limit_ns).  Draining in-flight copies after an
+// abort always uses this default.
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 struct Params {
   const float *q_descale;
@@ -40,6 +43,7 @@ struct Params {
   int k_per_token, v_per_head, causal;
   int q_ntd, kv_nhd;  // layouts: Q [N1, T, 128] (q_descale [N1, T]); pages [P, ps, N2, 128]
   int qd_tok, qd_head;  // q_descale element strides of a token and of a head
+  unsigned long long wait_limit_ns;  // a wait that runs longer aborts the launch
   float scale_log2;   // softmax_scale * log2(e)
   float log2_pscale;  // log2(p_scale)
   float ln_pscale;    // ln(p_scale)

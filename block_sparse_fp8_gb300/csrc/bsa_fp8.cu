@@ -13,6 +13,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -150,9 +151,14 @@ static bsa_status_t check_device(size_t attn_smem, int *num_sms, int *per_sm = n
   return BSA_OK;
 }
 
+// Limit of one bounded wait inside the prefill kernel; 0 selects the default.
+static std::atomic<unsigned long long> g_wait_limit_ns{0};
+
 static Params make_params(const bsa_fp8_dims_t *d) {
   Params p;
   memset(&p, 0, sizeof(p));
+  const unsigned long long lim = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p.wait_limit_ns = lim ? lim : WAIT_LIMIT_NS;
   p.B = d->B;
   p.N1 = d->N1;
   p.N2 = d->N2;
@@ -233,6 +239,11 @@ extern "C" size_t bsa_fp8_prefill_workspace_size(const bsa_fp8_dims_t *dims) {
   int num_sms = 0;
   if (check_device(0, &num_sms) != BSA_OK) return WORKSPACE_BYTES;
   return plan_splits(make_params(dims), num_sms, true).bytes;
+}
+
+extern "C" bsa_status_t bsa_fp8_set_wait_limit_ns(unsigned long long ns) {
+  g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+  return BSA_OK;
 }
 
 extern "C" const char *bsa_status_string(bsa_status_t status) {

@@ -32,7 +32,8 @@
  *     length outside its declared maximum) are reported by OR-ing BSA_DEV_* bits into
  *     *dev_status (if dev_status is not NULL) -- read it after synchronising.  The bad
  *     entry is skipped (a bad page reads as zeros); nothing traps or hangs.
- *   - Every wait inside the kernels is bounded; a wait that runs out sets BSA_DEV_TIMEOUT.
+ *   - Every wait inside the kernels is bounded (2 s, or bsa_fp8_set_wait_limit_ns); a wait
+ *     that runs out sets BSA_DEV_TIMEOUT.
  */
 #ifndef BSA_FP8_H
 #define BSA_FP8_H
@@ -249,6 +250,16 @@ bsa_status_t bsa_fp8_append_kv(const bsa_fp8_append_dims_t *dims, const void *k_
                                const int *cache_seqlens, const int *block_table,
                                const float *k_scale, const float *v_scale, void *k_pages,
                                void *v_pages, float *k_descale, int *dev_status, void *stream);
+
+/* Sets the limit of every bounded wait inside the prefill kernel for launches that follow, in
+ * nanoseconds, for the whole process; 0 restores the default of 2 s.  A wait that runs out
+ * sets BSA_DEV_TIMEOUT in *dev_status, every role of the CTA stops, waits (with the default
+ * limit) for the copies and tensor-core operations it has issued, frees its tensor memory and
+ * exits; the results of that launch are then undefined, the CUDA context stays usable.  A
+ * watchdog for callers that would rather get an error than wait on a stalled GPU; a limit
+ * below the kernel's legitimate waits (microseconds) aborts every launch.  No counterpart in
+ * the pages.  Always BSA_OK. */
+bsa_status_t bsa_fp8_set_wait_limit_ns(unsigned long long ns);
 
 /* Static text for a status code. */
 const char *bsa_status_string(bsa_status_t status);
