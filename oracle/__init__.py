@@ -96,6 +96,12 @@ def load(path: str | None = None):
                                                 ctypes.POINTER(OracleInputs), ctypes.c_int,
                                                 ctypes.c_int, ctypes.c_void_p, ctypes.c_long,
                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    lib.oracle_attention_rows_grouped.restype = ctypes.c_int
+    lib.oracle_attention_rows_grouped.argtypes = [ctypes.POINTER(OracleDims),
+                                                  ctypes.POINTER(OracleInputs), ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                                  ctypes.c_long, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_quantize_rows.restype = None
     lib.oracle_quantize_rows.argtypes = [ctypes.c_void_p, ctypes.c_long, ctypes.c_void_p,
@@ -137,25 +143,28 @@ class Oracle:
                                         _ptr(lists), _ptr(counts))
         return lists, counts, err
 
-    def rows(self, rows, mode=EXACT, nthreads=0, splits=1):
+    def rows(self, rows, mode=EXACT, nthreads=0, splits=1, group=1):
         """rows: int array [n, 2] of (token, head).  Returns (o [n,128] f64, lse [n] f64, err).
         splits > 1 (P-emulating mode): the active list cut into that many consecutive slices,
-        each with its own online softmax, merged by log-sum-exp weights."""
+        each with its own online softmax, merged by log-sum-exp weights.  group (P-emulating
+        mode): list tiles per online-softmax step, 1 (128-token tiles) or 2 (256-wide macro
+        blocks of two tiles, an odd last tile alone)."""
         rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
         n = rows.shape[0]
         o = np.zeros((n, 128), dtype=np.float64)
         lse = np.zeros(n, dtype=np.float64)
-        err = self.lib.oracle_attention_rows_split(ctypes.byref(self.dims),
-                                                   ctypes.byref(self.inputs), mode, int(splits),
-                                                   _ptr(rows), n, _ptr(o), _ptr(lse), nthreads)
+        err = self.lib.oracle_attention_rows_grouped(ctypes.byref(self.dims),
+                                                     ctypes.byref(self.inputs), mode,
+                                                     int(splits), int(group), _ptr(rows), n,
+                                                     _ptr(o), _ptr(lse), nthreads)
         return o, lse, err
 
-    def all_rows(self, mode=EXACT, nthreads=0, splits=1):
+    def all_rows(self, mode=EXACT, nthreads=0, splits=1, group=1):
         """Full O [T, N1, 128] and LSE [N1, T]."""
         c = self.case
         tok, h = np.meshgrid(np.arange(c.T), np.arange(c.N1), indexing="ij")
         rows = np.stack([tok.ravel(), h.ravel()], axis=1)
-        o, lse, err = self.rows(rows, mode, nthreads, splits)
+        o, lse, err = self.rows(rows, mode, nthreads, splits, group)
         return o.reshape(c.T, c.N1, 128), lse.reshape(c.T, c.N1).T.copy(), err
 
 

@@ -26,7 +26,9 @@
  * Two modes:
  *   ORACLE_EXACT (0): the formula itself in fp64 over the dequantised inputs.
  *   ORACLE_PEMU  (1): the tiled online softmax, one 128-token KV tile at a time in ascending
- *                     order, with P rounded to e4m3 at the fixed P-scale before the PV sum.
+ *                     order, with P rounded to e4m3 at the fixed P-scale before the PV sum;
+ *                     optionally two list tiles per step (the 256-wide macro block of
+ *                     [QBSA]'s kernel description) or the list in slices merged by LSE.
  *
  * Readings taken where the pages leave a step open (each is listed in the design notes):
  *   causal edge j <= i + (kv_len - q_len); KV head of query head h is h / (N1/N2);
@@ -229,23 +231,27 @@ static const uint8_t *kv_row(const oracle_dims_t *d, const uint8_t *pages, int p
 
 /* ------------------------------------------------------------------------------------
  * The P-emulating online softmax over the active tiles tiles[t_lo .. t_hi) of one row, in
- * order: per tile the running max m, alpha = exp(m_old - m), p = exp(x - m) in fp32, l from
- * the unrounded p, P * p_scale rounded to e4m3 for the P.V sum.  keys [na] are the row's
- * allowed keys in ascending order and s their logits.  Returns (m, l, acc) with acc the
- * un-normalised sum in P-scale units; m = -inf and l = 0 when nothing is visible.
+ * order, `group` consecutive list tiles per step (1: one 128-token tile at a time, [HPC]
+ * 固定 P-scale; 2: the 256-wide macro block of [QBSA]'s kernel description, two sparse
+ * 128-token blocks per step, an odd last tile alone): per step the running max m, alpha =
+ * exp(m_old - m), p = exp(x - m) in fp32, l from the unrounded p, P * p_scale rounded to
+ * e4m3 for the P.V sum.  keys [na] are the row's allowed keys in ascending order and s their
+ * logits.  Returns (m, l, acc) with acc the un-normalised sum in P-scale units; m = -inf and
+ * l = 0 when nothing is visible.
  * ------------------------------------------------------------------------------------ */
 static int pemu_slice(const oracle_dims_t *d, const oracle_inputs_t *in, int b, int g,
-                      const int *tiles, int t_lo, int t_hi, const int *keys, const double *s,
-                      int na, double *m_out, double *l_out, double *acc) {
+                      const int *tiles, int t_lo, int t_hi, int group, const int *keys,
+                      const double *s, int na, double *m_out, double *l_out, double *acc) {
   int err = 0;
   double m = -INFINITY, l = 0.0;
   for (int k = 0; k < HEAD_DIM; ++k) acc[k] = 0.0;
   int a = 0;
-  for (int ti = t_lo; ti < t_hi; ++ti) {
+  for (int ti = t_lo; ti < t_hi; ti += group) {
     int t0 = tiles[ti] * TILE;
+    int tl = tiles[(ti + group < t_hi ? ti + group : t_hi) - 1] * TILE;  /* the step's last tile */
     while (a < na && keys[a] < t0) ++a;              /* skip keys of earlier slices */
     int a0 = a;
-    while (a < na && keys[a] < t0 + TILE) ++a;       /* keys of this tile: [a0, a) */
+    while (a < na && keys[a] < tl + TILE) ++a;       /* keys of this step's tiles: [a0, a) */
     double mt = -INFINITY;
     for (int e = a0; e < a; ++e) {
       double x = (double)(float)s[e];                /* the logit as a 32-bit float */
@@ -282,7 +288,7 @@ static int pemu_slice(const oracle_dims_t *d, const oracle_inputs_t *in, int b, 
  * One output row (token tok of sequence b, query head h).
  * ------------------------------------------------------------------------------------ */
 static int one_row(const oracle_dims_t *d, const oracle_inputs_t *in, int mode, int splits,
-                   int tok, int h, double *o, double *lse) {
+                   int group, int tok, int h, double *o, double *lse) {
   int err = 0;
   int b = 0;
   while (b + 1 < d->B && in->cu_seqlens_q[b + 1] <= tok) ++b;
@@ -358,7 +364,7 @@ static int one_row(const oracle_dims_t *d, const oracle_inputs_t *in, int mode, 
     for (int c = 0; c < ns; ++c) {
       double mc, lc, accc[HEAD_DIM];
       err |= pemu_slice(d, in, b, g, tiles, (int)((long)c * nt / ns), (int)((long)(c + 1) * nt / ns),
-                        keys, s, na, &mc, &lc, accc);
+                        group, keys, s, na, &mc, &lc, accc);
       if (lc == 0.0 || mc == -INFINITY) continue;    /* an empty slice adds nothing */
       double mn = m > mc ? m : mc;
       double wo = (m == -INFINITY) ? 0.0 : exp(m - mn), wc = exp(mc - mn);
@@ -379,22 +385,32 @@ static int one_row(const oracle_dims_t *d, const oracle_inputs_t *in, int mode, 
   return err;
 }
 
-/* Rows given as (token, head) pairs; o [nrows, 128], lse [nrows].  Returns the OR of the data
- * errors met.  nthreads <= 0 means the OpenMP default. */
-int oracle_attention_rows_split(const oracle_dims_t *d, const oracle_inputs_t *in, int mode,
-                                int splits, const int *rows, long nrows, double *o, double *lse,
-                                int nthreads) {
+/* Rows given as (token, head) pairs; o [nrows, 128], lse [nrows].  In the P-emulating mode
+ * the list is cut into `splits` slices and each slice steps `group` list tiles at a time.
+ * Returns the OR of the data errors met.  nthreads <= 0 means the OpenMP default. */
+int oracle_attention_rows_grouped(const oracle_dims_t *d, const oracle_inputs_t *in, int mode,
+                                  int splits, int group, const int *rows, long nrows, double *o,
+                                  double *lse, int nthreads) {
   if (!d || !in || d->D != HEAD_DIM || d->N2 <= 0 || d->N1 % d->N2 != 0) return ORACLE_BAD_ARG;
   if (mode == ORACLE_PEMU && !(in->p_scale > 0.0)) return ORACLE_BAD_ARG;
+  if (group < 1) return ORACLE_BAD_ARG;
   int err = 0;
 #ifdef _OPENMP
   if (nthreads > 0) omp_set_num_threads(nthreads);
 #pragma omp parallel for schedule(dynamic, 16) reduction(| : err)
 #endif
   for (long r = 0; r < nrows; ++r)
-    err |= one_row(d, in, mode, splits, rows[2 * r], rows[2 * r + 1], o + r * HEAD_DIM, lse + r);
+    err |= one_row(d, in, mode, splits, group, rows[2 * r], rows[2 * r + 1], o + r * HEAD_DIM,
+                   lse + r);
   (void)nthreads;
   return err;
+}
+
+/* One 128-token tile per step. */
+int oracle_attention_rows_split(const oracle_dims_t *d, const oracle_inputs_t *in, int mode,
+                                int splits, const int *rows, long nrows, double *o, double *lse,
+                                int nthreads) {
+  return oracle_attention_rows_grouped(d, in, mode, splits, 1, rows, nrows, o, lse, nthreads);
 }
 
 /* The whole active list in one online softmax (splits = 1). */

@@ -495,6 +495,105 @@ def pin_fixed_pscale_running_max(lib):
     assert abs(o[255, 0, 3] - (1 + 2 * ee) / (1 + ee)) < 1e-12
 
 
+def _rising_tiles_case(ntiles):
+    """128·ntiles keys, one head, q = e0, softmax_scale 0.1, identity pages of 64.  Tile 0:
+    k = -e0 (s = -0.1), v = 1; tile 1: k = 0 (s = 0), v = 2; tile 2: k = -2e0 (s = -0.2),
+    v = 3; tile 3: k = e0 (s = 0.1), v = 4.  The row max rises at tile 1, so a step holding
+    tiles 0 and 1 quantises tile 0's P against tile 1's maximum."""
+    n = 128 * ntiles
+    q = np.zeros((n, 1, 128), np.uint8)
+    q[:, 0, 0] = 0x38                                     # 1.0
+    npages = 2 * ntiles
+    kp = np.zeros((npages, 1, 64, 128), np.uint8)
+    vp = np.zeros((npages, 1, 64, 128), np.uint8)
+    kcode = {0: 0xB8, 1: 0x00, 2: 0xC0, 3: 0x38}          # -1.0, 0, -2.0, 1.0
+    vcode = {0: 0x38, 1: 0x40, 2: 0x44, 3: 0x48}          # 1.0, 2.0, 3.0, 4.0
+    for t in range(ntiles):
+        kp[2 * t:2 * t + 2, 0, :, 0] = kcode[t]
+        vp[2 * t:2 * t + 2] = vcode[t]
+    return W.Case(name="rising", B=1, N1=1, N2=1, page_size=64, q_lens=[n], kv_lens=[n],
+                  k_scale_kind=0, v_scale_kind=0, causal=1, softmax_scale=0.1, p_scale=256.0,
+                  q=q, k_pages=kp, v_pages=vp, q_descale=np.ones((n, 1), np.float32),
+                  k_descale=np.ones(1, np.float32), v_descale=np.ones(1, np.float32),
+                  cu_seqlens_q=np.array([0, n], np.int32), seqused_kv=np.array([n], np.int32),
+                  block_table=np.arange(npages, dtype=np.int32)[None, :],
+                  block_mask=np.ones((1, 1, ntiles, ntiles), np.uint8))
+
+
+def pin_macro_block_pairs(lib):
+    """Two tiles, the last row sees both (s = -0.1 on tile 0, 0 on tile 1).  One tile per
+    step: tile 0 is quantised against its own maximum (p = 1 -> 256 exactly), then rescaled
+    by e^-0.1 when tile 1 raises the maximum, which gives the exact answer (2 + e)/(1 + e),
+    e = e^-0.1.  Both tiles in one step (the 256-wide macro block): tile 0's p = e^-0.1 is
+    scaled to 231.64 and rounds to 224, so O = (128*224*1 + 128*256*2) / (256*128 (1 + e)) =
+    736 / (256 (1 + e)).  LSE = ln(128 (1 + e)) either way; row 127 sees tile 0 only: O = 1."""
+    case = _rising_tiles_case(2)
+    e = math.exp(float(np.float32(-0.1)))
+    a = _oracle(case, lib)
+    o2, l2, _ = a.all_rows(O.PEMU, group=2)
+    assert abs(o2[255, 0, 5] - 736.0 / (256.0 * (1 + e))) < 1e-6
+    assert abs(l2[0, 255] - math.log(128 * (1 + e))) < 1e-6
+    assert abs(o2[127, 0, 5] - 1.0) < 1e-12
+    o1, _, _ = a.all_rows(O.PEMU, group=1)
+    assert abs(o1[255, 0, 5] - (2 + e) / (1 + e)) < 1e-6
+
+
+def pin_macro_block_odd_tail(lib):
+    """Three tiles (s = -0.1, 0, -0.2; v = 1, 2, 3), the last row sees all of them.  Two per
+    step: tiles 0 and 1 share the maximum 0 (224 and 256, as above); tile 2 is a step of its
+    own, below the maximum, p = e^-0.2 scaled to 209.59, which rounds to 208.  O = 128 (224*1 +
+    256*2 + 208*3) / (256*128 (e1 + 1 + e2)) = 1360 / (256 (e1 + 1 + e2)), e1 = e^-0.1,
+    e2 = e^-0.2."""
+    case = _rising_tiles_case(3)
+    e1 = math.exp(float(np.float32(-0.1)))
+    e2 = math.exp(float(np.float32(-0.2)))
+    o, lse, _ = _oracle(case, lib).all_rows(O.PEMU, group=2)
+    assert abs(o[383, 0, 7] - 1360.0 / (256.0 * (e1 + 1 + e2))) < 1e-6
+    assert abs(lse[0, 383] - math.log(128 * (e1 + 1 + e2))) < 1e-6
+
+
+def pin_macro_block_second_pair(lib):
+    """Four tiles (s = -0.1, 0, -0.2, 0.1; v = 1, 2, 3, 4), the last row sees all of them, in
+    steps (0, 1), (2, 3).  Step 1: maximum 0, P = 224 and 256 as above, l1 = 128 (e1 + 1).
+    Step 2: the maximum rises to 0.1, a = e^-0.1; tile 2's p = e^-0.3 scaled to 189.65 rounds
+    to 192, tile 3's p = 1 gives 256.  O = (a*128*736 + 128 (192*3 + 256*4)) /
+    (256 (a*l1 + 128 (e3 + 1))), e3 = e^-0.3; LSE = 0.1 + ln(a*l1 + 128 (e3 + 1))."""
+    case = _rising_tiles_case(4)
+    f = lambda x: float(np.float32(x))
+    e1 = math.exp(f(-0.1))
+    a = math.exp(-f(0.1))
+    e3 = float(np.float32(math.exp(f(-0.2) - f(0.1))))
+    l1 = 128 * (float(np.float32(e1)) + 1)
+    lt = a * l1 + 128 * (e3 + 1)
+    o, lse, _ = _oracle(case, lib).all_rows(O.PEMU, group=2)
+    assert abs(o[511, 0, 11] - (a * 128 * 736 + 128 * (192 * 3 + 256 * 4)) / (256 * lt)) < 1e-6
+    assert abs(lse[0, 511] - (f(0.1) + math.log(lt))) < 1e-6
+
+
+def pin_macro_block_closed_form_zero_k(lib):
+    """K = 0: every visible key has p = 1 whatever the grouping, so two tiles per step gives
+    the plain mean of the visible V and LSE = ln |A_i|, as the exact formula does."""
+    case = _uniform_k_case(31)
+    a = _oracle(case, lib)
+    o2, l2, _ = a.all_rows(O.PEMU, group=2)
+    oe, le, _ = a.all_rows(O.EXACT)
+    _close(o2, oe, 1e-9)
+    _close(l2, le, 1e-9)
+
+
+def pin_macro_block_near_exact(lib):
+    """Two tiles per step stays within the exact band on a random block-sparse case."""
+    case = W.make_case("macro", 32, [700, 300], [700, 300], 4, 2, 64, 1, 2, "bernoulli",
+                       keep=0.6)
+    a = _oracle(case, lib)
+    o2, l2, _ = a.all_rows(O.PEMU, group=2)
+    oe, le, _ = a.all_rows(O.EXACT)
+    bad = np.abs(o2 - oe) > 0.02 + 0.02 * np.abs(oe)
+    assert bad.mean() < 0.005
+    seen = le > -1e30
+    assert np.all(np.abs(l2[seen] - le[seen]) <= 2.5e-5 + 0.005 * np.abs(le[seen]))
+
+
 def pin_pemu_near_exact(lib):
     """The e4m3-rounded P stays within the exact band on all but a sliver of elements."""
     case = W.make_case("pe", 41, [512], [512], 4, 1, 64, W.SCALE_PER_TOKEN_HEAD,

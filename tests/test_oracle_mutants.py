@@ -43,6 +43,11 @@ MUTANTS = {
                               "(double)(float)(p * in->p_scale))) / in->p_scale;"),
     "pemu_exact_p_in_pv": ("tile_acc[k] += pq * oracle_e4m3_decode(vr[k]);",
                            "tile_acc[k] += p * in->p_scale * oracle_e4m3_decode(vr[k]);"),
+    "macro_group_steps_by_one": ("for (int ti = t_lo; ti < t_hi; ti += group) {",
+                                 "for (int ti = t_lo; ti < t_hi; ti += 1) {"),
+    "macro_group_first_tile_only": (
+        "int tl = tiles[(ti + group < t_hi ? ti + group : t_hi) - 1] * TILE;",
+        "int tl = t0;"),
     "split_merge_weight_sign": ("double wo = (m == -INFINITY) ? 0.0 : exp(m - mn), wc = exp(mc - mn);",
                                 "double wo = (m == -INFINITY) ? 0.0 : exp(m - mn), wc = exp(mn - mc);"),
     "split_slice_keeps_earlier_keys": (
