@@ -42,6 +42,9 @@ METRIC = ("block-sparse FP8 prefill effective TFLOPS (active tiles) and ms/call,
 DEFAULT_WORKLOAD = "varlen_4x16k_h64kv8_idx25"
 OTHER_WORKLOADS = ("prefill_2x8k_h32kv8_bsm50_outliers", "chunked_4k_over_64k_h32kv4_local_sink",
                    "dense_32k_h32kv8")
+# workloads also timed with 256-wide macro blocks (two list tiles per online-softmax step)
+MACRO_WORKLOADS = ("varlen_4x16k_h64kv8_idx25", "prefill_2x8k_h32kv8_bsm50_outliers",
+                   "dense_32k_h32kv8")
 FP8_PER_BF16 = 2.0        # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
@@ -59,6 +62,11 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-others", action="store_true",
                     help="skip the other full-size workloads (profiling runs)")
+    ap.add_argument("--no-macro", action="store_true",
+                    help="skip the 256-wide macro-block timings")
+    ap.add_argument("--tiles-per-step", type=int, default=1, choices=[1, 2],
+                    help="online-softmax step of the timed prefill: one 128-token tile, or a "
+                         "256-wide macro block of two")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--op", choices=["prefill", "quantize"], default="prefill",
                     help="prefill (the hot path, default) or the quantise step that feeds it: "
@@ -271,6 +279,34 @@ def make_workload(args):
     return W.make_case(args.workload, **kw)
 
 
+def time_steps(step, steps, warmup, flush, stream, dev):
+    """Per-step CUDA-event times (ms) of `steps` calls of step(), L2 flushed before each."""
+    import torch
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    per = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        per.append(e0.elapsed_time(e1))
+    return per
+
+
+def macro_line(per, flops, fp8_peak):
+    """The 256-wide macro-block run of a workload, timed like the 128-wide one."""
+    ms = statistics.mean(per)
+    return {"ms_per_call": {"mean": ms, "median": statistics.median(per), "min": min(per)},
+            "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "roofline_frac": flops / (ms * 1e-3) / 1e12 / fp8_peak,
+            "kernel": "bsa_attention_wide_kernel"}
+
+
 def upload(case, dev):
     import torch
 
@@ -283,7 +319,7 @@ def upload(case, dev):
                 sparse_seq_len=t(case.sparse_seq_len))
 
 
-def time_other_workload(name, steps, warmup, dev, flush, fp8_peak, traffic_of):
+def time_other_workload(name, steps, warmup, dev, flush, fp8_peak, traffic_of, macro=False):
     """One more full-size workload timed like the main one (L2 flushed before every step,
     CUDA events around each call); its buffers are freed before returning."""
     import torch
@@ -304,7 +340,7 @@ def time_other_workload(name, steps, warmup, dev, flush, fp8_peak, traffic_of):
     workspace = torch.empty(max(bsa.workspace_size(dims), 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def step(tiles_per_step=1):
         bsa.prefill(d["q"], d["k_pages"], d["v_pages"], d["q_descale"], d["k_descale"],
                     d["v_descale"], d["cu_seqlens_q"], d["seqused_kv"], d["block_table"],
                     case.max_q_len, case.max_kv_len, block_mask=d["block_mask"],
@@ -312,20 +348,10 @@ def time_other_workload(name, steps, warmup, dev, flush, fp8_peak, traffic_of):
                     softmax_scale=case.softmax_scale, p_scale=case.p_scale,
                     causal=bool(case.causal), out=out, lse=lse, dev_status=status,
                     workspace=workspace, stream=stream, k_scale_kind=case.k_scale_kind,
-                    v_scale_kind=case.v_scale_kind)
+                    v_scale_kind=case.v_scale_kind, tiles_per_step=tiles_per_step)
 
-    for _ in range(warmup):
-        flush.zero_()
-        step()
-    per = []
-    for _ in range(steps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        per.append(e0.elapsed_time(e1))
+    per = time_steps(step, steps, warmup, flush, stream, dev)
+    per2 = time_steps(lambda: step(2), steps, warmup, flush, stream, dev) if macro else None
     if int(status.item()) != 0:
         raise RuntimeError(f"{name}: device status {int(status.item())}")
     ms = statistics.mean(per)
@@ -338,6 +364,8 @@ def time_other_workload(name, steps, warmup, dev, flush, fp8_peak, traffic_of):
            "config": config_of(case, name, tiles, flops)}
     if "fa_convention_gflop" in res["config"]:
         res["fa_convention_tflops"] = res["config"]["fa_convention_gflop"] * 1e9 / (ms * 1e-3) / 1e12
+    if per2 is not None:
+        res["macro_block_256"] = macro_line(per2, flops, fp8_peak)
     del d, out, lse, workspace
     torch.cuda.empty_cache()
     return res
@@ -386,7 +414,7 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def step():
+    def step(tiles_per_step=args.tiles_per_step):
         bsa.prefill(d["q"], d["k_pages"], d["v_pages"], d["q_descale"], d["k_descale"],
                     d["v_descale"], d["cu_seqlens_q"], d["seqused_kv"], d["block_table"],
                     case.max_q_len, case.max_kv_len, block_mask=d["block_mask"],
@@ -394,7 +422,7 @@ def run_ours(args, rank, world):
                     softmax_scale=case.softmax_scale, p_scale=case.p_scale,
                     causal=bool(case.causal), out=out, lse=lse, dev_status=status,
                     workspace=workspace, stream=stream, k_scale_kind=case.k_scale_kind,
-                    v_scale_kind=case.v_scale_kind)
+                    v_scale_kind=case.v_scale_kind, tiles_per_step=tiles_per_step)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -447,6 +475,17 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize(dev)
         warm.append(w0.elapsed_time(w1))
 
+    # the same workload with 256-wide macro blocks (two list tiles per online-softmax step),
+    # timed the same way after the timed region
+    macro = None
+    if (not args.no_macro and args.tiles_per_step == 1 and args.batch == 0 and
+            args.workload in MACRO_WORKLOADS):
+        per2 = time_steps(lambda: step(2), max(5, min(args.steps, 20)), max(args.warmup, 3),
+                          flush, stream, dev)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} (macro blocks)")
+        macro = per2
+
     # end to end through the public API: host (pinned) inputs in, host output back, every
     # step.  Two buffer sets and three streams let step i's copy-in, step i-1's prefill and
     # step i-2's copy-out overlap, as a serving loop would run them; each step still copies
@@ -487,7 +526,7 @@ def run_ours(args, rank, world):
                         sparse_seq_len=di["sparse_seq_len"], softmax_scale=case.softmax_scale,
                         p_scale=case.p_scale, causal=bool(case.causal), out=o_b, lse=l_b,
                         workspace=workspace, stream=stream, k_scale_kind=case.k_scale_kind,
-                        v_scale_kind=case.v_scale_kind)
+                        v_scale_kind=case.v_scale_kind, tiles_per_step=args.tiles_per_step)
             ev_run[bset].record(stream)
             s_out.wait_event(ev_run[bset])
             with torch.cuda.stream(s_out):
@@ -583,6 +622,11 @@ def run_ours(args, rank, world):
     if "fa_convention_gflop" in line["config"]:
         line["fa_convention_tflops"] = (weak_scaling_value(world, line["config"]["fa_convention_gflop"] * 1e9, ms)
                                         / 1e12)
+    if args.tiles_per_step == 2:
+        line["config"]["tiles_per_step"] = 2
+        line["roofline"]["kernel"] = "bsa_attention_wide_kernel"
+    if macro is not None:
+        line["macro_block_256"] = macro_line(macro, flops, fp8_peak)
     if not args.no_cpu_baseline and world >= 1:
         line["cpu_baseline"] = cpu_baseline(case, lists, counts, args.cpu_seconds)
     if not args.no_others and args.batch == 0:
@@ -593,7 +637,8 @@ def run_ours(args, rank, world):
         steps = max(5, min(args.steps, 20))
         line["other_workloads"] = {
             name: time_other_workload(name, steps, max(args.warmup, 3), dev, flush, fp8_peak,
-                                      measured_traffic)
+                                      measured_traffic,
+                                      macro=not args.no_macro and name in MACRO_WORKLOADS)
             for name in OTHER_WORKLOADS if name != args.workload}
     return line
 

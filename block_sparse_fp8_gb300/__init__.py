@@ -44,7 +44,7 @@ class Dims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "B", "N1", "N2", "D", "page_size", "max_q_len", "max_kv_len", "num_pages",
         "max_pages_per_seq", "total_q", "k_scale_kind", "v_scale_kind", "causal", "q_layout",
-        "kv_layout")]
+        "kv_layout", "tiles_per_step")]
 
 
 Q_TND, Q_NTD = 0, 1
@@ -113,7 +113,8 @@ def _stream_handle(stream):
 
 
 def make_dims(q, k_pages, block_table, cu_seqlens_q, max_q_len, max_kv_len, k_scale_kind,
-              v_scale_kind, causal=True, q_layout=Q_TND, kv_layout=KV_HND) -> Dims:
+              v_scale_kind, causal=True, q_layout=Q_TND, kv_layout=KV_HND,
+              tiles_per_step=1) -> Dims:
     if q_layout == Q_NTD:
         N1, T, D = q.shape
     else:
@@ -126,7 +127,8 @@ def make_dims(q, k_pages, block_table, cu_seqlens_q, max_q_len, max_kv_len, k_sc
                 max_q_len=int(max_q_len), max_kv_len=int(max_kv_len), num_pages=P,
                 max_pages_per_seq=block_table.shape[1], total_q=T,
                 k_scale_kind=int(k_scale_kind), v_scale_kind=int(v_scale_kind),
-                causal=int(bool(causal)), q_layout=int(q_layout), kv_layout=int(kv_layout))
+                causal=int(bool(causal)), q_layout=int(q_layout), kv_layout=int(kv_layout),
+                tiles_per_step=int(tiles_per_step))
 
 
 def workspace_size(dims: Dims) -> int:
@@ -138,7 +140,8 @@ def prefill(q, k_pages, v_pages, q_descale, k_descale, v_descale, cu_seqlens_q, 
             sparse_seq_len=None, softmax_scale: float | None = None, p_scale: float = 256.0,
             causal: bool = True, out=None, lse=None, return_lse: bool = True, dev_status=None,
             workspace=None, stream=None, k_scale_kind: int | None = None,
-            v_scale_kind: int | None = None, q_layout: int = Q_TND, kv_layout: int = KV_HND):
+            v_scale_kind: int | None = None, q_layout: int = Q_TND, kv_layout: int = KV_HND,
+            tiles_per_step: int = 1):
     """Block-sparse FP8 prefill.  Tensors are CUDA tensors in the C ABI's layouts:
     q uint8/float8_e4m3fn [T, N1, 128] (q_layout Q_TND) or [N1, T, 128] (Q_NTD, with q_descale
     [N1, T]); k_pages, v_pages [P, N2, page, 128] (KV_HND) or [P, page, N2, 128] (KV_NHD);
@@ -149,7 +152,8 @@ def prefill(q, k_pages, v_pages, q_descale, k_descale, v_descale, cu_seqlens_q, 
     max_q_len / max_kv_len are host integers (upper bounds of the per-sequence lengths).
     The scale kinds default to what the descale shapes imply (K [P, N2, page] = per token and
     head; V [N2] = per head, which for N2 = 1 is the same as per tensor).
-    Returns (out bf16 [T, N1, 128], lse f32 [N1, T] or None)."""
+    tiles_per_step = 2 runs the online softmax over 256-wide macro blocks (two list tiles
+    per step).  Returns (out bf16 [T, N1, 128], lse f32 [N1, T] or None)."""
     import torch
 
     n2 = k_pages.shape[2] if kv_layout == KV_NHD else k_pages.shape[1]
@@ -158,7 +162,7 @@ def prefill(q, k_pages, v_pages, q_descale, k_descale, v_descale, cu_seqlens_q, 
     v_kind = v_scale_kind if v_scale_kind is not None else (
         SCALE_PER_HEAD if v_descale.numel() == n2 else SCALE_PER_TENSOR)
     dims = make_dims(q, k_pages, block_table, cu_seqlens_q, max_q_len, max_kv_len, k_kind,
-                     v_kind, causal, q_layout, kv_layout)
+                     v_kind, causal, q_layout, kv_layout, tiles_per_step)
     T, N1, D = dims.total_q, dims.N1, dims.D
     if out is None:
         out = torch.empty((T, N1, D), dtype=torch.bfloat16, device=q.device)

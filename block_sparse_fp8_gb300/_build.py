@@ -12,7 +12,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libbsa_fp8.so")
 SOURCES = [os.path.join(CSRC, "bsa_fp8.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("ptx_sm103.cuh", "bsa_common.cuh", "bsa_attention.cuh",
-                                           "bsa_quant.cuh")] + [
+                                           "bsa_attention_wide.cuh", "bsa_quant.cuh")] + [
     os.path.join(INCLUDE, "bsa_fp8.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

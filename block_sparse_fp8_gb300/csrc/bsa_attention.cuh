@@ -99,7 +99,8 @@ static_assert(sizeof(Smem) + NPIPE * kb_pad(KB_MAX) * sizeof(uint16_t) + 1024 <=
 
 // Bounded mbarrier wait.  On timeout: report, raise the pipeline's abort flag and return false.
 // Returns false without waiting once another role of the pipeline has aborted.
-__device__ __forceinline__ bool wait_bar(const Params &p, Pipe &s, uint64_t *bar,
+template <typename PipeT>
+__device__ __forceinline__ bool wait_bar(const Params &p, PipeT &s, uint64_t *bar,
                                          uint32_t parity) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -120,13 +121,15 @@ __device__ __forceinline__ bool wait_bar(const Params &p, Pipe &s, uint64_t *bar
 
 // The softmax warps' waits after a first failed test, out of line so that their hot path
 // carries only the test (the smaller loop body measurably helps the softmax).
-__device__ __noinline__ bool wait_bar_warp_slow(const Params &p, Pipe &s, uint64_t *bar,
+template <typename PipeT>
+__device__ __noinline__ bool wait_bar_warp_slow(const Params &p, PipeT &s, uint64_t *bar,
                                                 uint32_t parity) {
   return __all_sync(0xffffffffu, wait_bar(p, s, bar, parity));
 }
 
 // Warp-uniform version for code followed by warp-collective instructions.
-__device__ __forceinline__ bool wait_bar_warp(const Params &p, Pipe &s, uint64_t *bar,
+template <typename PipeT>
+__device__ __forceinline__ bool wait_bar_warp(const Params &p, PipeT &s, uint64_t *bar,
                                               uint32_t parity) {
   if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
   return wait_bar_warp_slow(p, s, bar, parity);

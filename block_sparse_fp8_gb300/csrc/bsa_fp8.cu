@@ -20,6 +20,7 @@
 #include <mutex>
 
 #include "bsa_attention.cuh"
+#include "bsa_attention_wide.cuh"
 #include "bsa_common.cuh"
 #include "bsa_fp8.h"
 #include "bsa_quant.cuh"
@@ -88,6 +89,7 @@ static bsa_status_t validate_dims(const bsa_fp8_dims_t *d) {
   if (d->causal != 0 && d->causal != 1) return BSA_ERR_INVALID_ARGUMENT;
   if (d->q_layout != BSA_Q_TND && d->q_layout != BSA_Q_NTD) return BSA_ERR_INVALID_ARGUMENT;
   if (d->kv_layout != BSA_KV_HND && d->kv_layout != BSA_KV_NHD) return BSA_ERR_INVALID_ARGUMENT;
+  if (d->tiles_per_step < 0 || d->tiles_per_step > 2) return BSA_ERR_INVALID_ARGUMENT;
   if (cdiv(d->max_kv_len, TILE) > KB_MAX) return BSA_ERR_UNSUPPORTED;
   // task indices are int; the work-item counter runs past the last task by up to one claim
   // per pipeline, so keep the count well inside int range
@@ -102,13 +104,15 @@ struct DeviceInfo {
   int smem_per_sm = 0;        // shared memory of one SM
   int smem_reserved = 0;      // shared memory the system reserves per resident block
   size_t smem_attr = 0;  // dynamic shared memory the attention kernel is enabled for
+  size_t smem_attr_wide = 0;  // ... and the 256-wide macro-block kernel
 };
 
 static DeviceInfo g_devices[64];
 static std::mutex g_devices_mu;
 
 // sm_103 only; caches the SM count and raises the attention kernel's shared-memory limit.
-static bsa_status_t check_device(size_t attn_smem, int *num_sms, int *per_sm = nullptr) {
+static bsa_status_t check_device(size_t attn_smem, int *num_sms, int *per_sm = nullptr,
+                                 bool wide = false) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
   if (dev < 0 || dev >= 64) return BSA_ERR_UNSUPPORTED;
@@ -132,19 +136,25 @@ static bsa_status_t check_device(size_t attn_smem, int *num_sms, int *per_sm = n
       // The softmax warpgroups raise their registers with setmaxnreg.inc, drawing on what the
       // CTA was launched with; that only completes if the launch allocation covers the
       // whole split, so refuse to launch a build where it does not.
-      cudaFuncAttributes fa;
-      if (cudaFuncGetAttributes(&fa, attn::bsa_attention_kernel) != cudaSuccess)
+      cudaFuncAttributes fa, fw;
+      if (cudaFuncGetAttributes(&fa, attn::bsa_attention_kernel) != cudaSuccess ||
+          cudaFuncGetAttributes(&fw, attn_wide::bsa_attention_wide_kernel) != cudaSuccess)
         return BSA_ERR_CUDA;
-      if (fa.numRegs * attn::NTHREADS < attn::SPLIT_REGS) di.state = 2;
+      if (fa.numRegs * attn::NTHREADS < attn::SPLIT_REGS ||
+          fw.numRegs * attn_wide::NTHREADS < attn_wide::SPLIT_REGS)
+        di.state = 2;
     }
   }
   if (di.state != 1) return BSA_ERR_UNSUPPORTED;
-  if (attn_smem > di.smem_attr) {
-    if (cudaFuncSetAttribute(attn::bsa_attention_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)attn_smem) != cudaSuccess)
-      return BSA_ERR_CUDA;
-    di.smem_attr = attn_smem;
+  size_t &attr = wide ? di.smem_attr_wide : di.smem_attr;
+  if (attn_smem > attr) {
+    const cudaError_t e =
+        wide ? cudaFuncSetAttribute(attn_wide::bsa_attention_wide_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem)
+             : cudaFuncSetAttribute(attn::bsa_attention_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem);
+    if (e != cudaSuccess) return BSA_ERR_CUDA;
+    attr = attn_smem;
   }
   if (num_sms) *num_sms = di.num_sms;
   if (per_sm) *per_sm = 1;  // one CTA per SM: it holds the SM's registers and all of TMEM
@@ -238,7 +248,7 @@ extern "C" size_t bsa_fp8_prefill_workspace_size(const bsa_fp8_dims_t *dims) {
   if (validate_dims(dims) != BSA_OK) return 0;
   int num_sms = 0;
   if (check_device(0, &num_sms) != BSA_OK) return WORKSPACE_BYTES;
-  return plan_splits(make_params(dims), num_sms, true).bytes;
+  return plan_splits(make_params(dims), num_sms, dims->tiles_per_step != 2).bytes;
 }
 
 extern "C" bsa_status_t bsa_fp8_set_wait_limit_ns(unsigned long long ns) {
@@ -393,9 +403,11 @@ static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, cons
   if (!noalloc && (!workspace || workspace_bytes < WORKSPACE_BYTES ||
                    (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0))
     return BSA_ERR_WORKSPACE;
-  const size_t smem = attn::smem_bytes(p.Kb);
+  // 256-wide macro blocks (two list tiles per online-softmax step) run their own kernel
+  const bool wide = dims->tiles_per_step == 2;
+  const size_t smem = wide ? attn_wide::smem_bytes(p.Kb) : attn::smem_bytes(p.Kb);
   int num_sms = 0, per_sm = 1;
-  st = check_device(smem, &num_sms, &per_sm);
+  st = check_device(smem, &num_sms, &per_sm, wide);
   if (st != BSA_OK) return st;
   if (noalloc) {
     // the library's own array, looked up only once every argument has been checked
@@ -403,8 +415,9 @@ static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, cons
     if (st != BSA_OK) return st;
     workspace_bytes = NOALLOC_SCRATCH_BYTES;
   }
-  // the array-backed entry point never splits: its array holds the item counter only
-  const SplitPlan plan = plan_splits(p, num_sms, !noalloc);
+  // the array-backed entry point never splits: its array holds the item counter only; nor do
+  // macro blocks (a slice boundary would cut a pair)
+  const SplitPlan plan = plan_splits(p, num_sms, !noalloc && !wide);
   if (workspace_bytes < plan.bytes ||
       (plan.splits > 1 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
     return BSA_ERR_WORKSPACE;
@@ -469,8 +482,12 @@ static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, cons
   const size_t zero_bytes = plan.splits > 1 ? plan.off_ml : sizeof(int);
   if (cudaMemsetAsync(workspace, 0, zero_bytes, (cudaStream_t)stream) != cudaSuccess)
     return BSA_ERR_CUDA;
-  attn::bsa_attention_kernel<<<(unsigned)grid, attn::NTHREADS, smem, (cudaStream_t)stream>>>(
-      p, tq, tk, tv);
+  if (wide)
+    attn_wide::bsa_attention_wide_kernel<<<(unsigned)grid, attn_wide::NTHREADS, smem,
+                                           (cudaStream_t)stream>>>(p, tq, tk, tv);
+  else
+    attn::bsa_attention_kernel<<<(unsigned)grid, attn::NTHREADS, smem, (cudaStream_t)stream>>>(
+        p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 

@@ -98,6 +98,11 @@ typedef struct {
   int causal;            /* 1 = right-context causal (mask_mode 3), 0 = no causal mask (mode 0) */
   int q_layout;          /* BSA_Q_TND (0) or BSA_Q_NTD (1) */
   int kv_layout;         /* BSA_KV_HND (0) or BSA_KV_NHD (1) */
+  int tiles_per_step;    /* active-list tiles per online-softmax step: 1 (or 0) = one 128-token
+                            tile; 2 = a 256-wide macro block of two consecutive list tiles, an
+                            odd last tile alone (Quant Block Sparse Attention, kernel
+                            description): the row maximum that P is quantised against, and the
+                            rescale of O, move once per pair.  2 never uses split-KV. */
 } bsa_fp8_dims_t;
 
 #define BSA_Q_TND 0

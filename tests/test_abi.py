@@ -70,7 +70,8 @@ def _prefill(L, dims, **ptrs):
     dict(D=64), dict(page_size=48), dict(page_size=128), dict(N1=6, N2=4), dict(N1=34, N2=2),
     dict(N1=0), dict(N2=0), dict(max_q_len=-1), dict(max_kv_len=-5), dict(total_q=-1),
     dict(max_pages_per_seq=15), dict(k_scale_kind=2), dict(v_scale_kind=1),
-    dict(causal=2), dict(B=-1), dict(q_layout=2), dict(kv_layout=-1)])
+    dict(causal=2), dict(B=-1), dict(q_layout=2), dict(kv_layout=-1), dict(tiles_per_step=3),
+    dict(tiles_per_step=-1)])
 def test_invalid_dims(L, bad):
     assert _prefill(L, _dims(**bad)) == INVALID
 
