@@ -717,8 +717,7 @@ __device__ __forceinline__ void run_softmax(const Params &p, Pipe &s, uint32_t t
         // O *= alpha on this thread's 64 columns
         const uint64_t a2 = ptx::pk(alpha, alpha);
         uint32_t o[2][32];
-        ptx::tmem_ld16x2_32<64>(tO, o[0]);
-        ptx::tmem_ld16x2_32<64>(tO + 32, o[1]);
+        ptx::tmem_ld16x2_64<64>(tO, o[0], o[1]);
         ptx::tmem_ld_wait(o[0]);
         ptx::reg_fence(o[1]);
 #pragma unroll

@@ -105,6 +105,10 @@ __device__ int compact_task(const Params &p, int b, int h, int qt, int kend, Out
       n += __popc(bal);
     }
   } else if (p.sparse_indices) {
+    // the first 32 entries of the row are read together with its length (they lie inside the
+    // [B, N1, Qb, Kb] row whatever the length), so a list of up to 32 entries costs one round
+    // trip to memory instead of two
+    const int first = lane < p.Kb ? p.sparse_indices[row + lane] : -1;
     int len = p.sparse_seq_len[task];
     if (len < 0 || len > p.Kb) {
       if (lane == 0) report(p, BSA_DEV_BAD_INDEX);
@@ -114,7 +118,7 @@ __device__ int compact_task(const Params &p, int b, int h, int qt, int kend, Out
     for (int w = lane; w < nwords; w += 32) bitmap[w] = 0u;
     __syncwarp();
     for (int e = lane; e < len; e += 32) {
-      int t = p.sparse_indices[row + e];
+      const int t = e < 32 ? first : p.sparse_indices[row + e];
       if (t < 0 || t >= p.Kb)
         report(p, BSA_DEV_BAD_INDEX);
       else if (t < kend)
