@@ -2,7 +2,8 @@
 
 A thin ctypes binding over the C ABI in include/bsa_fp8.h: it marshals PyTorch CUDA tensors
 (device pointers) and the current stream into ``bsa_fp8_prefill`` / ``bsa_fp8_compact_tiles``
-and the quantise step ``bsa_fp8_quantize_rows`` / ``bsa_fp8_append_kv``.
+and the quantise step ``bsa_fp8_quantize_rows`` / ``bsa_fp8_append_kv``; ``prefill_host``
+marshals CPU tensors into ``bsa_fp8_prefill_host``, which copies them in and the results out.
 Every step of the computation runs in the library's CUDA kernels; there is no CPU path.
 The library must have been built (``block_sparse_fp8_gb300._build.build()``); importing the
 binding on a machine without it raises immediately.
@@ -15,7 +16,8 @@ import os
 
 from . import _build
 
-__all__ = ["Dims", "AppendDims", "Q_TND", "Q_NTD", "KV_HND", "KV_NHD", "prefill", "compact_tiles", "quantize_rows", "append_kv",
+__all__ = ["Dims", "AppendDims", "Tensors", "TENSOR_NAMES", "Q_TND", "Q_NTD", "KV_HND",
+           "KV_NHD", "prefill", "prefill_host", "compact_tiles", "quantize_rows", "append_kv",
            "workspace_size", "status_string", "set_wait_limit_ns", "lib",
            "SCALE_PER_TENSOR", "SCALE_PER_TOKEN_HEAD", "SCALE_PER_HEAD", "BsaError",
            "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_BAD_SEQLEN", "DEV_TIMEOUT"]
@@ -30,8 +32,8 @@ DEV_BAD_SEQLEN = 4
 DEV_TIMEOUT = 8
 
 EXPORTED = ("bsa_fp8_prefill", "bsa_fp8_prefill_workspace_size", "bsa_fp8_compact_tiles",
-            "bsa_fp8_prefill_noalloc", "bsa_fp8_quantize_rows", "bsa_fp8_append_kv",
-            "bsa_fp8_set_wait_limit_ns", "bsa_status_string")
+            "bsa_fp8_prefill_noalloc", "bsa_fp8_prefill_host", "bsa_fp8_quantize_rows",
+            "bsa_fp8_append_kv", "bsa_fp8_set_wait_limit_ns", "bsa_status_string")
 
 
 class BsaError(RuntimeError):
@@ -45,6 +47,16 @@ class Dims(ctypes.Structure):
         "B", "N1", "N2", "D", "page_size", "max_q_len", "max_kv_len", "num_pages",
         "max_pages_per_seq", "total_q", "k_scale_kind", "v_scale_kind", "causal", "q_layout",
         "kv_layout", "tiles_per_step")]
+
+
+# the tensors of one call, in bsa_fp8_tensors_t's order (prefill's argument names; out, lse)
+TENSOR_NAMES = ("q", "k_pages", "v_pages", "q_descale", "k_descale", "v_descale",
+                "cu_seqlens_q", "seqused_kv", "block_table", "block_mask", "sparse_indices",
+                "sparse_seq_len", "out", "lse")
+
+
+class Tensors(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in TENSOR_NAMES]
 
 
 Q_TND, Q_NTD = 0, 1
@@ -77,6 +89,9 @@ def lib():
         L.bsa_fp8_prefill_noalloc.restype = i32
         L.bsa_fp8_prefill_noalloc.argtypes = [ctypes.POINTER(Dims)] + [vp] * 12 + [f32, f32, vp,
                                                                                   vp, vp, vp]
+        L.bsa_fp8_prefill_host.restype = i32
+        L.bsa_fp8_prefill_host.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Tensors),
+                                           ctypes.POINTER(Tensors), f32, f32, vp, sz, vp, vp]
         L.bsa_fp8_compact_tiles.restype = i32
         L.bsa_fp8_compact_tiles.argtypes = [ctypes.POINTER(Dims)] + [vp] * 9
         L.bsa_fp8_quantize_rows.restype = i32
@@ -181,6 +196,41 @@ def prefill(q, k_pages, v_pages, q_descale, k_descale, v_descale, cu_seqlens_q, 
     if st != 0:
         raise BsaError(st, "bsa_fp8_prefill")
     return out, lse
+
+
+def prefill_host(host: dict, dev: dict, max_q_len: int, max_kv_len: int,
+                 softmax_scale: float | None = None, p_scale: float = 256.0, causal: bool = True,
+                 workspace=None, dev_status=None, stream=None, k_scale_kind: int | None = None,
+                 v_scale_kind: int | None = None, q_layout: int = Q_TND,
+                 kv_layout: int = KV_HND, tiles_per_step: int = 1) -> None:
+    """The prefill on host tensors (bsa_fp8_prefill_host).  `host` maps the names in
+    TENSOR_NAMES to CPU tensors (page-locked ones make the copies asynchronous; absent or None
+    = not given); "out" and "lse" receive the results once `stream` has been synchronised.
+    `dev` maps the same names to CUDA tensors of the same shapes, which the call fills and
+    computes on.  Scale kinds default as in prefill()."""
+    import torch
+
+    k_descale, v_descale = host["k_descale"], host["v_descale"]
+    k_pages = host["k_pages"]
+    n2 = k_pages.shape[2] if kv_layout == KV_NHD else k_pages.shape[1]
+    k_kind = k_scale_kind if k_scale_kind is not None else (
+        SCALE_PER_TOKEN_HEAD if k_descale.dim() == 3 else SCALE_PER_TENSOR)
+    v_kind = v_scale_kind if v_scale_kind is not None else (
+        SCALE_PER_HEAD if v_descale.numel() == n2 else SCALE_PER_TENSOR)
+    dims = make_dims(host["q"], k_pages, host["block_table"], host["cu_seqlens_q"], max_q_len,
+                     max_kv_len, k_kind, v_kind, causal, q_layout, kv_layout, tiles_per_step)
+    ws_bytes = workspace_size(dims)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev["q"].device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(dims.D)
+    th = Tensors(*(_p(host.get(n)) for n in TENSOR_NAMES))
+    td = Tensors(*(_p(dev.get(n)) for n in TENSOR_NAMES))
+    st = lib().bsa_fp8_prefill_host(ctypes.byref(dims), ctypes.byref(th), ctypes.byref(td),
+                                    float(softmax_scale), float(p_scale), _p(workspace),
+                                    ws_bytes, _p(dev_status), _stream_handle(stream))
+    if st != 0:
+        raise BsaError(st, "bsa_fp8_prefill_host")
 
 
 def compact_tiles(cu_seqlens_q, seqused_kv, dims: Dims, block_mask=None, sparse_indices=None,

@@ -372,7 +372,7 @@ bsa_status_t noalloc_scratch(void **addr) {
 
 // The prefill.  With `noalloc` it ignores workspace / workspace_bytes and uses the library's
 // own array instead (never split-KV); otherwise the caller's workspace must hold the split
-// plan's bytes.
+// plan's bytes.  With `check_only` it returns after every check, before anything is queued.
 static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, const void *k_pages,
                                  const void *v_pages, const float *q_descale,
                                  const float *k_descale, const float *v_descale,
@@ -381,7 +381,8 @@ static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, cons
                                  const int *sparse_indices, const int *sparse_seq_len,
                                  float softmax_scale, float p_scale, void *out_bf16,
                                  float *lse_f32, void *workspace, size_t workspace_bytes,
-                                 int *dev_status, void *stream, bool noalloc) {
+                                 int *dev_status, void *stream, bool noalloc,
+                                 bool check_only = false) {
   bsa_status_t st = validate_dims(dims);
   if (st != BSA_OK) return st;
   if (block_mask && sparse_indices) return BSA_ERR_INVALID_ARGUMENT;
@@ -421,6 +422,7 @@ static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, cons
   if (workspace_bytes < plan.bytes ||
       (plan.splits > 1 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
     return BSA_ERR_WORKSPACE;
+  if (check_only) return BSA_OK;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   p.splits = plan.splits;
   if (plan.splits > 1) {
@@ -505,6 +507,73 @@ extern "C" bsa_status_t bsa_fp8_prefill(const bsa_fp8_dims_t *dims, const void *
                       seqused_kv, block_table, block_mask, sparse_indices, sparse_seq_len,
                       softmax_scale, p_scale, out_bf16, lse_f32, workspace, workspace_bytes,
                       dev_status, stream, false);
+}
+
+extern "C" bsa_status_t bsa_fp8_prefill_host(const bsa_fp8_dims_t *dims,
+                                             const bsa_fp8_tensors_t *host,
+                                             const bsa_fp8_tensors_t *dev, float softmax_scale,
+                                             float p_scale, void *workspace,
+                                             size_t workspace_bytes, int *dev_status,
+                                             void *stream) {
+  if (!host || !dev) return BSA_ERR_INVALID_ARGUMENT;
+  bsa_status_t st = validate_dims(dims);
+  if (st != BSA_OK) return st;
+  const Params p = make_params(dims);
+  // an empty problem queues nothing, as bsa_fp8_prefill launches nothing for it
+  const bool empty = (long long)p.B * p.N1 * p.Qb == 0 || p.T == 0;
+  // every tensor of the device set has its host counterpart, and the reverse
+  if (!empty && (!host->q || !host->k_pages || !host->v_pages || !host->q_descale ||
+                 !host->k_descale || !host->v_descale || !host->cu_seqlens_q ||
+                 !host->block_table || !host->out_bf16))
+    return BSA_ERR_INVALID_ARGUMENT;
+  if (!empty && (!host->seqused_kv != !dev->seqused_kv || !host->block_mask != !dev->block_mask ||
+                 !host->sparse_indices != !dev->sparse_indices ||
+                 !host->sparse_seq_len != !dev->sparse_seq_len || !host->lse_f32 != !dev->lse_f32))
+    return BSA_ERR_INVALID_ARGUMENT;
+  const auto run = [&](bool check_only) {
+    return prefill_impl(dims, dev->q, dev->k_pages, dev->v_pages, dev->q_descale,
+                        dev->k_descale, dev->v_descale, dev->cu_seqlens_q, dev->seqused_kv,
+                        dev->block_table, dev->block_mask, dev->sparse_indices,
+                        dev->sparse_seq_len, softmax_scale, p_scale, dev->out_bf16,
+                        dev->lse_f32, workspace, workspace_bytes, dev_status, stream, false,
+                        check_only);
+  };
+  st = run(true);
+  if (st != BSA_OK || empty) return st;
+
+  const size_t T = (size_t)p.T, N1 = (size_t)p.N1, N2 = (size_t)p.N2, B = (size_t)p.B;
+  const size_t cache_rows = (size_t)p.num_pages * N2 * (size_t)p.ps;
+  const size_t tasks = B * N1 * (size_t)p.Qb;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const auto copy = [&](const void *dst, const void *src, size_t bytes, cudaMemcpyKind kind) {
+    if (!src || bytes == 0) return true;
+    if (cudaMemcpyAsync(const_cast<void *>(dst), src, bytes, kind, s) == cudaSuccess) return true;
+    cudaGetLastError();  // leave no pending error behind
+    return false;
+  };
+  const cudaMemcpyKind in = cudaMemcpyHostToDevice;
+  const bool queued =
+      copy(dev->q, host->q, T * N1 * HEAD_DIM, in) &&
+      copy(dev->k_pages, host->k_pages, cache_rows * HEAD_DIM, in) &&
+      copy(dev->v_pages, host->v_pages, cache_rows * HEAD_DIM, in) &&
+      copy(dev->q_descale, host->q_descale, T * N1 * sizeof(float), in) &&
+      copy(dev->k_descale, host->k_descale, (p.k_per_token ? cache_rows : 1) * sizeof(float),
+           in) &&
+      copy(dev->v_descale, host->v_descale, (p.v_per_head ? N2 : 1) * sizeof(float), in) &&
+      copy(dev->cu_seqlens_q, host->cu_seqlens_q, (B + 1) * sizeof(int), in) &&
+      copy(dev->seqused_kv, host->seqused_kv, B * sizeof(int), in) &&
+      copy(dev->block_table, host->block_table, B * (size_t)p.L * sizeof(int), in) &&
+      copy(dev->block_mask, host->block_mask, tasks * (size_t)p.Kb, in) &&
+      copy(dev->sparse_indices, host->sparse_indices, tasks * (size_t)p.Kb * sizeof(int), in) &&
+      copy(dev->sparse_seq_len, host->sparse_seq_len, tasks * sizeof(int), in);
+  if (!queued) return BSA_ERR_CUDA;
+  st = run(false);
+  if (st != BSA_OK) return st;
+  const cudaMemcpyKind out = cudaMemcpyDeviceToHost;
+  if (!copy(host->out_bf16, dev->out_bf16, T * N1 * HEAD_DIM * 2, out) ||
+      !copy(host->lse_f32, dev->lse_f32, N1 * T * sizeof(float), out))
+    return BSA_ERR_CUDA;
+  return BSA_OK;
 }
 
 // ------------------------------------------------------------------------------------------

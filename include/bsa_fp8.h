@@ -207,6 +207,53 @@ bsa_status_t bsa_fp8_prefill_noalloc(const bsa_fp8_dims_t *dims, const void *q,
                                      float p_scale, void *out_bf16, float *lse_f32,
                                      int *dev_status, void *stream);
 
+/* The tensors of one prefill call, by the names and layouts bsa_fp8_prefill gives them. */
+typedef struct {
+  const void *q;
+  const void *k_pages;
+  const void *v_pages;
+  const float *q_descale;
+  const float *k_descale;
+  const float *v_descale;
+  const int *cu_seqlens_q;
+  const int *seqused_kv;      /* or NULL */
+  const int *block_table;
+  const uint8_t *block_mask;  /* or NULL */
+  const int *sparse_indices;  /* or NULL */
+  const int *sparse_seq_len;  /* or NULL */
+  void *out_bf16;
+  float *lse_f32;             /* or NULL */
+} bsa_fp8_tensors_t;
+
+/* bsa_fp8_prefill on inputs and outputs in HOST memory.
+ *
+ * `host` holds every tensor in host memory and `dev` a device buffer of the same size for
+ * each tensor `host` gives (the optional ones NULL in both, or given in both).  On `stream`
+ * the call queues: one host-to-device copy per input tensor (host -> dev), the prefill on
+ * the `dev` tensors exactly as bsa_fp8_prefill runs it, then the device-to-host copies of
+ * O and, when given, the LSE (dev -> host).  It returns once they are queued; the host
+ * outputs are valid after the stream has been synchronised.  Sizes come from `dims`:
+ *   q, out            T * N1 * 128 bytes (out: * 2, bf16)
+ *   k_pages, v_pages  num_pages * N2 * page_size * 128 bytes
+ *   q_descale         T * N1 floats;  lse  N1 * T floats
+ *   k_descale         1 float, or num_pages * N2 * page_size (BSA_SCALE_PER_TOKEN_HEAD)
+ *   v_descale         1 float, or N2 (BSA_SCALE_PER_HEAD)
+ *   cu_seqlens_q      B + 1 ints;  seqused_kv  B ints;  block_table  B * max_pages_per_seq
+ *   block_mask        B * N1 * Qb * Kb bytes;  sparse_indices  B * N1 * Qb * Kb ints;
+ *   sparse_seq_len    B * N1 * Qb ints
+ * Host buffers in page-locked memory (cudaHostAlloc / cudaHostRegister) make the copies
+ * asynchronous, so that calls on two streams with separate `dev` sets and workspaces overlap
+ * one call's copies with the other's prefill; pageable host memory gives the same results.
+ * Every argument is checked, as bsa_fp8_prefill checks the `dev` set, before anything is
+ * queued: BSA_ERR_INVALID_ARGUMENT for a NULL host pointer, a tensor given on one side only,
+ * or what bsa_fp8_prefill rejects; BSA_ERR_CUDA if a copy cannot be queued.  `workspace` and
+ * `dev_status` are device memory, as for bsa_fp8_prefill.  No counterpart in the pages: the
+ * host-to-host path a caller without device buffers of its own inputs runs. */
+bsa_status_t bsa_fp8_prefill_host(const bsa_fp8_dims_t *dims, const bsa_fp8_tensors_t *host,
+                                  const bsa_fp8_tensors_t *dev, float softmax_scale,
+                                  float p_scale, void *workspace, size_t workspace_bytes,
+                                  int *dev_status, void *stream);
+
 /* ------------------------------------------------------------------------------------------
  * The quantise step before the attention call: bf16 inputs into the e4m3 + descale format
  * above.  Rule (FlashMLA page, section 量化 / 解量化的源码实现, applied per 128-element row

@@ -165,3 +165,54 @@ def test_noalloc_scalar_pointer_and_size_checks(L):
     assert _noalloc(L, _dims(max_kv_len=4097 * 128, max_pages_per_seq=4097 * 2,
                              num_pages=8194)) == UNSUPPORTED
     assert _noalloc(L, _dims(B=0, total_q=0)) == 0
+
+
+def _host(L, dims, host=None, dev=None, **over):
+    """bsa_fp8_prefill_host with fake addresses (never dereferenced: every case below fails
+    validation before a copy is queued).  `over` sets "host.<name>" / "dev.<name>"."""
+    fake = 0x10000
+    sets = {}
+    for side in ("host", "dev"):
+        t = dict.fromkeys(bsa.TENSOR_NAMES, fake)
+        t.update(block_mask=None, sparse_indices=None, sparse_seq_len=None)
+        for key, val in over.items():
+            s, name = key.split(".")
+            if s == side:
+                t[name] = val
+        sets[side] = bsa.Tensors(*(t[n] for n in bsa.TENSOR_NAMES))
+    h = None if host == "null" else ctypes.byref(sets["host"])
+    d = None if dev == "null" else ctypes.byref(sets["dev"])
+    return L.bsa_fp8_prefill_host(ctypes.byref(dims), h, d, 0.088, 256.0, fake, 256, None, None)
+
+
+@pytest.mark.parametrize("bad", [dict(D=64), dict(page_size=48), dict(N1=6, N2=4),
+                                 dict(max_pages_per_seq=15), dict(tiles_per_step=3)])
+def test_host_call_validates_dims_like_prefill(L, bad):
+    d = _dims(**bad)
+    assert _host(L, d) == _prefill(L, d) == INVALID
+
+
+def test_host_call_tensor_checks(L):
+    d = _dims()
+    assert _host(L, d, host="null") == INVALID
+    assert _host(L, d, dev="null") == INVALID
+    for name in ("q", "k_pages", "v_pages", "q_descale", "k_descale", "v_descale",
+                 "cu_seqlens_q", "block_table", "out"):
+        assert _host(L, d, **{f"host.{name}": None}) == INVALID, name   # host side missing
+        assert _host(L, d, **{f"dev.{name}": None}) == INVALID, name    # device side missing
+    for name in ("seqused_kv", "lse"):   # optional tensors: given on both sides or neither
+        assert _host(L, d, **{f"host.{name}": None}) == INVALID, name
+        assert _host(L, d, **{f"dev.{name}": None}) == INVALID, name
+    assert _host(L, d, **{"host.block_mask": 0x20000}) == INVALID
+    assert _host(L, d, **{"dev.sparse_indices": 0x20000, "dev.sparse_seq_len": 0x30000}) == INVALID
+    assert _host(L, d, **{"dev.q": 0x10001}) == INVALID                 # the device set's alignment
+    assert _host(L, d, **{"host.block_mask": 0x20000, "dev.block_mask": 0x30000,
+                          "host.sparse_indices": 0x20000, "dev.sparse_indices": 0x30000,
+                          "host.sparse_seq_len": 0x20000,
+                          "dev.sparse_seq_len": 0x30000}) == INVALID    # both sparse forms
+
+
+def test_host_call_empty_problem_is_a_no_op(L):
+    nothing = {f"{s}.{n}": None for s in ("host", "dev") for n in bsa.TENSOR_NAMES}
+    assert _host(L, _dims(B=0, total_q=0), **nothing) == 0
+    assert _host(L, _dims(total_q=0), **nothing) == 0

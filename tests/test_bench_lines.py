@@ -47,6 +47,7 @@ def test_prefill_line():
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert e["host_link"]["h2d_gbs"] > 0 and e["host_link"]["d2h_gbs"] > 0
+    assert e["call"].startswith("bsa_fp8_prefill_host")
     assert d["warm_l2_ms_per_call"]["median"] > 0
     assert "sm_mhz" in d["clocks"]
     # the other full-size workloads, timed the same way, in the same line
