@@ -104,10 +104,10 @@ def load(path: str | None = None):
                                                   ctypes.c_void_p, ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_quantize_rows.restype = None
-    lib.oracle_quantize_rows.argtypes = [ctypes.c_void_p, ctypes.c_long, ctypes.c_void_p,
-                                         ctypes.c_void_p]
+    lib.oracle_quantize_rows.argtypes = [ctypes.c_void_p, ctypes.c_long, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_void_p]
     lib.oracle_append_kv.restype = ctypes.c_int
-    lib.oracle_append_kv.argtypes = [ctypes.c_int] * 7 + [ctypes.c_void_p] * 10
+    lib.oracle_append_kv.argtypes = [ctypes.c_int] * 8 + [ctypes.c_void_p] * 10
     if path is None:
         _lib = lib
     return lib
@@ -168,23 +168,29 @@ class Oracle:
         return o.reshape(c.T, c.N1, 128), lse.reshape(c.T, c.N1).T.copy(), err
 
 
-def quantize_rows(x_bf16: np.ndarray, lib=None):
+DESCALE_AMAX, DESCALE_UE8M0 = 0, 1
+
+
+def quantize_rows(x_bf16: np.ndarray, lib=None, rule: int = DESCALE_AMAX):
     """x_bf16: uint16 bf16 bit patterns [..., 128].  Returns (codes uint8 [..., 128], descale
-    float32 [...]): per row descale = amax/448 (1 for a zero row), code = e4m3(x / descale)."""
+    float32 [...]): per row descale = amax/448 (1 for a zero row), with DESCALE_UE8M0 rounded
+    up to a power of two (FlashMLA page, 量化 / 解量化的源码实现), code = e4m3(x / descale)."""
     lib = lib if lib is not None else load()
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     assert x.shape[-1] == 128
     rows = x.size // 128
     codes = np.zeros(x.shape, dtype=np.uint8)
     desc = np.zeros(x.shape[:-1], dtype=np.float32)
-    lib.oracle_quantize_rows(_ptr(x), rows, _ptr(codes), _ptr(desc))
+    lib.oracle_quantize_rows(_ptr(x), rows, int(rule), _ptr(codes), _ptr(desc))
     return codes, desc
 
 
 def append_kv(k_new, v_new, cu_new, cache_len, block_table, k_pages, v_pages, k_descale,
-              k_scale_kind, v_scale_kind, k_scale=None, v_scale=None, lib=None):
+              k_scale_kind, v_scale_kind, k_scale=None, v_scale=None, lib=None,
+              k_descale_rule: int = DESCALE_AMAX):
     """Writes bf16 K/V tokens [T_new, N2, 128] (uint16 bit patterns) into copies of the paged
-    cache arrays.  Returns (k_pages, v_pages, k_descale, err)."""
+    cache arrays; per-token K descales follow k_descale_rule.  Returns (k_pages, v_pages,
+    k_descale, err)."""
     lib = lib if lib is not None else load()
     k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
     v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
@@ -199,6 +205,7 @@ def append_kv(k_new, v_new, cu_new, cache_len, block_table, k_pages, v_pages, k_
     P, N2, ps, D = kp.shape
     B = cu_new.size - 1
     err = lib.oracle_append_kv(B, N2, ps, P, bt.shape[1], int(k_scale_kind), int(v_scale_kind),
+                               int(k_descale_rule),
                                _ptr(k_new), _ptr(v_new), _ptr(cu_new), _ptr(cache_len), _ptr(bt),
                                _ptr(ks), _ptr(vs), _ptr(kp), _ptr(vp), _ptr(kd))
     return kp, vp, kd, err

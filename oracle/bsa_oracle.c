@@ -60,6 +60,10 @@
 #define SCALE_PER_TOKEN_HEAD 1
 #define SCALE_PER_HEAD 2
 
+/* descale rules of the quantise step */
+#define ORACLE_DESCALE_AMAX 0    /* amax / 448 */
+#define ORACLE_DESCALE_UE8M0 1   /* amax / 448 rounded up to a power of two */
+
 /* error codes returned by the oracle (data the pages call invalid) */
 #define ORACLE_OK 0
 #define ORACLE_BAD_INDEX 1       /* sparse index outside [0, Kb) or sparse_seq_len outside [0, Kb] */
@@ -434,10 +438,12 @@ int oracle_max_threads(void) {
  * tile: the scale is the tile's largest absolute value over 448 (the largest finite e4m3)
  * and the stored value is e4m3(x / scale).  The attention pages give Q per token per head,
  * K per token per head (or per tensor) and V per head (or per tensor) descales, i.e. the
- * same rule applied to each 128-element row of Q and K.  Readings: no rounding of the scale
- * to a power of two (that step belongs to FlashMLA's own cache format); an all-zero row gets
- * descale 1 and zero codes; both divisions are fp32 divisions (the precision of the inputs'
- * consumers); e4m3 rounds to nearest even and saturates (oracle_e4m3_encode).
+ * same rule applied to each 128-element row of Q and K.  Readings: by default the scale is
+ * not rounded (ORACLE_DESCALE_AMAX); with ORACLE_DESCALE_UE8M0 it is rounded up to a power of
+ * two, FlashMLA's cast of the scale to UE8M0 (the same section: the smallest 2^k not below
+ * amax / 448, so that multiplying a code by the scale is exact); an all-zero row gets descale
+ * 1 and zero codes under either rule; both divisions are fp32 divisions (the precision of the
+ * inputs' consumers); e4m3 rounds to nearest even and saturates (oracle_e4m3_encode).
  * ------------------------------------------------------------------------------------ */
 static float bf16_value(uint16_t b) {
   uint32_t u = (uint32_t)b << 16;
@@ -446,14 +452,24 @@ static float bf16_value(uint16_t b) {
   return f;
 }
 
+/* The smallest power of two not below x (x > 0, finite): frexpf writes x = m * 2^e with m in
+ * [0.5, 1), so x is itself a power of two exactly when m = 0.5, and otherwise 2^e is the next
+ * one up.  Subnormal x are handled by frexpf like any other. */
+static float pow2_ceil(float x) {
+  int e;
+  float m = frexpf(x, &e);
+  return m == 0.5f ? x : ldexpf(1.0f, e);
+}
+
 /* One row of 128 bf16 values -> 128 codes; returns the row's descale. */
-static float quantize_row(const uint16_t *x, uint8_t *codes) {
+static float quantize_row(const uint16_t *x, uint8_t *codes, int rule) {
   float amax = 0.0f;
   for (int i = 0; i < HEAD_DIM; ++i) {
     float a = fabsf(bf16_value(x[i]));
     if (a > amax) amax = a;
   }
   float descale = amax > 0.0f ? amax / 448.0f : 1.0f;
+  if (rule == ORACLE_DESCALE_UE8M0 && amax > 0.0f) descale = pow2_ceil(descale);
   for (int i = 0; i < HEAD_DIM; ++i) {
     float v = bf16_value(x[i]) / descale;
     codes[i] = oracle_e4m3_encode((double)v);
@@ -462,21 +478,24 @@ static float quantize_row(const uint16_t *x, uint8_t *codes) {
 }
 
 /* x [rows, 128] bf16 -> codes [rows, 128] e4m3, descale [rows] (Q [T, N1, 128] gives the
- * q_descale layout [T, N1] directly). */
-void oracle_quantize_rows(const uint16_t *x, long rows, uint8_t *codes, float *descale) {
+ * q_descale layout [T, N1] directly); rule = ORACLE_DESCALE_AMAX or ORACLE_DESCALE_UE8M0. */
+void oracle_quantize_rows(const uint16_t *x, long rows, int rule, uint8_t *codes,
+                          float *descale) {
   for (long r = 0; r < rows; ++r)
-    descale[r] = quantize_row(x + r * HEAD_DIM, codes + r * HEAD_DIM);
+    descale[r] = quantize_row(x + r * HEAD_DIM, codes + r * HEAD_DIM, rule);
 }
 
 /* Writes new K/V tokens into the paged cache.  Token i of sequence b (rows cu_new[b] + i of
  * k_new / v_new [T_new, N2, 128] bf16) lands at logical position pos = cache_len[b] + i, i.e.
  * page block_table[b, pos / page_size], slot pos % page_size of [P, N2, page_size, 128].
- * K: with SCALE_PER_TOKEN_HEAD each (token, head) row is quantised as above and its descale
- * stored in k_descale [P, N2, page_size]; with SCALE_PER_TENSOR the codes are e4m3(x / k_scale)
+ * K: with SCALE_PER_TOKEN_HEAD each (token, head) row is quantised as above (under
+ * k_descale_rule) and its descale stored in k_descale [P, N2, page_size]; with
+ * SCALE_PER_TENSOR the codes are e4m3(x / k_scale)
  * with the caller's k_scale.  V: e4m3(x / v_scale[head]) (SCALE_PER_HEAD) or / v_scale[0].
  * A token whose page is missing or outside [0, num_pages) is skipped and reported. */
 int oracle_append_kv(int B, int N2, int page_size, int num_pages, int max_pages_per_seq,
-                     int k_scale_kind, int v_scale_kind, const uint16_t *k_new,
+                     int k_scale_kind, int v_scale_kind, int k_descale_rule,
+                     const uint16_t *k_new,
                      const uint16_t *v_new, const int *cu_new, const int *cache_len,
                      const int *block_table, const float *k_scale, const float *v_scale,
                      uint8_t *k_pages, uint8_t *v_pages, float *k_descale) {
@@ -496,7 +515,7 @@ int oracle_append_kv(int B, int N2, int page_size, int num_pages, int max_pages_
         size_t src = ((size_t)(cu_new[b] + i) * N2 + g) * HEAD_DIM;
         size_t row = ((size_t)pg * N2 + g) * page_size + slot;
         if (k_scale_kind == SCALE_PER_TOKEN_HEAD) {
-          k_descale[row] = quantize_row(k_new + src, k_pages + row * HEAD_DIM);
+          k_descale[row] = quantize_row(k_new + src, k_pages + row * HEAD_DIM, k_descale_rule);
         } else {
           for (int e = 0; e < HEAD_DIM; ++e)
             k_pages[row * HEAD_DIM + e] =

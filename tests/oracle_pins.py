@@ -725,6 +725,51 @@ def pin_quantize_closed_forms(lib):
     assert np.all(np.abs(deq - x) <= bound)
 
 
+def pin_quantize_ue8m0_closed_forms(lib):
+    """FlashMLA's cast of the scale to UE8M0 (FlashMLA page, 量化 / 解量化的源码实现): the
+    descale is the smallest power of two not below amax / 448, worked by hand per row."""
+    vals = np.zeros((6, 128), dtype=np.float32)
+    vals[0, :3] = [448.0, -224.0, 1.0]   # amax / 448 = 1 is a power of two: descale 1
+    vals[1, :2] = [450.0, -1.0]          # 450 / 448 just above 1 (449 is no bf16): descale
+    #                                      2; 225 -> 224
+    vals[2, 0] = 1.0                     # 1 / 448 in (2^-9, 2^-8): descale 2^-8, 1 -> 256
+    vals[3, :2] = [300.0, 100.0]         # 300 / 448 in (1/2, 1): descale 1; 300 -> 288, 100 -> 96
+    # row 4 stays zero: descale 1, zero codes, as under the plain rule
+    xb = f32_to_bf16_bits(vals)
+    xb[5, 0] = 0x0001                    # 2^-133, the smallest bf16: amax / 448 is an fp32
+    #                                      subnormal (146 * 2^-149), descale 2^-141, code of 256
+    codes, desc = O.quantize_rows(xb, lib=lib, rule=O.DESCALE_UE8M0)
+    assert list(desc) == [1.0, 2.0, 2.0 ** -8, 1.0, 1.0, 2.0 ** -141], list(desc)
+    assert list(codes[0, :3]) == [0x7E, 0xF6, 0x38]
+    assert list(codes[1, :2]) == [0x76, 0xB0]
+    assert codes[2, 0] == 0x78 and codes[5, 0] == 0x78
+    assert list(codes[3, :2]) == [0x79, 0x6C]
+    assert not codes[4].any()
+    for r in range(6):
+        assert not codes[r, 3:].any()
+
+
+def pin_quantize_ue8m0_invariants(lib):
+    """On rows spanning 2^-120 .. 2^120: every UE8M0 descale is a power of two in
+    [amax/448, 2 amax/448) (amax/448 as an fp32 quotient), the codes are torch's e4m3 cast of
+    x / descale, and each row's largest code decodes to [224, 448] (amax / descale lies in
+    (224, 448] and rounds to no less than 224)."""
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((64, 128)).astype(np.float32)
+    x *= (2.0 ** rng.integers(-120, 120, size=(64, 1))).astype(np.float32)
+    xb = f32_to_bf16_bits(x)
+    codes, desc = O.quantize_rows(xb, lib=lib, rule=O.DESCALE_UE8M0)
+    xf = bf16_bits_to_f32(xb)
+    base = (np.abs(xf).max(axis=1) / np.float32(448.0)).astype(np.float32)
+    lg = np.log2(desc.astype(np.float64))
+    assert np.all(lg == np.round(lg)), "not a power of two"
+    assert np.all(desc >= base) and np.all(desc / 2 < base)
+    for r in range(64):
+        assert np.array_equal(codes[r], _torch_codes(xf[r], desc[r])), r
+    big = np.abs(torch_decode(codes)).max(axis=1)
+    assert np.all(big >= 224.0) and np.all(big <= 448.0)
+
+
 def _append_fixture(k_kind, v_kind):
     rng = np.random.default_rng(99)
     P, N2, ps = 9, 2, 4
@@ -754,12 +799,13 @@ def _torch_codes(x, scale):
 
 
 def pin_append_kv_placement(lib):
-    for k_kind, v_kind in ((W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD),
-                           (W.SCALE_PER_TENSOR, W.SCALE_PER_TENSOR)):
+    for k_kind, v_kind, rule in ((W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD, O.DESCALE_AMAX),
+                                 (W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD, O.DESCALE_UE8M0),
+                                 (W.SCALE_PER_TENSOR, W.SCALE_PER_TENSOR, O.DESCALE_AMAX)):
         f = _append_fixture(k_kind, v_kind)
         kp, vp, kd, err = O.append_kv(f["kb"], f["vb"], f["cu_new"], f["cache_len"], f["bt"],
                                       f["kp"], f["vp"], f["kd"], k_kind, v_kind,
-                                      f["k_scale"], f["v_scale"], lib=lib)
+                                      f["k_scale"], f["v_scale"], lib=lib, k_descale_rule=rule)
         assert err == 0
         ps = f["ps"]
         written = np.zeros(kp.shape[:3], dtype=bool)
@@ -772,8 +818,12 @@ def pin_append_kv_placement(lib):
                 slot = pos % ps
                 for g in range(2):
                     written[pg, g, slot] = True
-                    if k_kind == W.SCALE_PER_TOKEN_HEAD:
+                    if k_kind == W.SCALE_PER_TOKEN_HEAD and rule == O.DESCALE_AMAX:
                         c, d = torch_quantize_rows(f["kb"][tok, g][None])
+                        assert np.array_equal(kp[pg, g, slot], c[0]) and kd[pg, g, slot] == d[0]
+                    elif k_kind == W.SCALE_PER_TOKEN_HEAD:
+                        # the row's own quantisation under the same rule, checked above
+                        c, d = O.quantize_rows(f["kb"][tok, g][None], lib=lib, rule=rule)
                         assert np.array_equal(kp[pg, g, slot], c[0]) and kd[pg, g, slot] == d[0]
                     else:
                         assert np.array_equal(kp[pg, g, slot], _torch_codes(kx[tok, g], f["k_scale"][0]))

@@ -53,6 +53,12 @@ MUTANTS = {
     "split_slice_keeps_earlier_keys": (
         "    while (a < na && keys[a] < t0) ++a;              /* skip keys of earlier slices */",
         ""),
+    "ue8m0_round_down": ("return m == 0.5f ? x : ldexpf(1.0f, e);",
+                         "return m == 0.5f ? x : ldexpf(1.0f, e - 1);"),
+    "ue8m0_rule_ignored": (
+        "if (rule == ORACLE_DESCALE_UE8M0 && amax > 0.0f) descale = pow2_ceil(descale);", ""),
+    "ue8m0_always_next_power": ("return m == 0.5f ? x : ldexpf(1.0f, e);",
+                                "return ldexpf(1.0f, e);"),
     "quant_wrong_max": ("float descale = amax > 0.0f ? amax / 448.0f : 1.0f;",
                         "float descale = amax > 0.0f ? amax / 240.0f : 1.0f;"),
     "quant_zero_row_descale": ("float descale = amax > 0.0f ? amax / 448.0f : 1.0f;",
