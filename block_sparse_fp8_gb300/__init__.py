@@ -20,6 +20,7 @@ __all__ = ["Dims", "AppendDims", "Tensors", "TENSOR_NAMES", "Q_TND", "Q_NTD", "K
            "KV_NHD", "prefill", "prefill_host", "compact_tiles", "quantize_rows", "append_kv",
            "workspace_size", "status_string", "set_wait_limit_ns", "lib",
            "SCALE_PER_TENSOR", "SCALE_PER_TOKEN_HEAD", "SCALE_PER_HEAD", "BsaError",
+           "DESCALE_AMAX", "DESCALE_UE8M0",
            "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_BAD_SEQLEN", "DEV_TIMEOUT"]
 
 SCALE_PER_TENSOR = 0
@@ -33,7 +34,12 @@ DEV_TIMEOUT = 8
 
 EXPORTED = ("bsa_fp8_prefill", "bsa_fp8_prefill_workspace_size", "bsa_fp8_compact_tiles",
             "bsa_fp8_prefill_noalloc", "bsa_fp8_prefill_host", "bsa_fp8_quantize_rows",
-            "bsa_fp8_append_kv", "bsa_fp8_set_wait_limit_ns", "bsa_status_string")
+            "bsa_fp8_quantize_rows_ue8m0", "bsa_fp8_append_kv", "bsa_fp8_set_wait_limit_ns",
+            "bsa_status_string")
+
+# descale rules of the quantise step
+DESCALE_AMAX = 0    # amax / 448
+DESCALE_UE8M0 = 1   # amax / 448 rounded up to a power of two
 
 
 class BsaError(RuntimeError):
@@ -66,7 +72,7 @@ KV_HND, KV_NHD = 0, 1
 class AppendDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "B", "N2", "D", "page_size", "num_pages", "max_pages_per_seq", "total_new",
-        "k_scale_kind", "v_scale_kind", "kv_layout")]
+        "k_scale_kind", "v_scale_kind", "kv_layout", "k_descale_rule")]
 
 
 _lib = None
@@ -96,6 +102,8 @@ def lib():
         L.bsa_fp8_compact_tiles.argtypes = [ctypes.POINTER(Dims)] + [vp] * 9
         L.bsa_fp8_quantize_rows.restype = i32
         L.bsa_fp8_quantize_rows.argtypes = [vp, ctypes.c_longlong, vp, vp, vp]
+        L.bsa_fp8_quantize_rows_ue8m0.restype = i32
+        L.bsa_fp8_quantize_rows_ue8m0.argtypes = [vp, ctypes.c_longlong, vp, vp, vp]
         L.bsa_fp8_append_kv.restype = i32
         L.bsa_fp8_append_kv.argtypes = [ctypes.POINTER(AppendDims)] + [vp] * 12
         L.bsa_fp8_set_wait_limit_ns.restype = i32
@@ -252,9 +260,10 @@ def compact_tiles(cu_seqlens_q, seqused_kv, dims: Dims, block_mask=None, sparse_
     return lists, counts
 
 
-def quantize_rows(x, codes=None, descale=None, stream=None):
+def quantize_rows(x, codes=None, descale=None, stream=None, rule: int = DESCALE_AMAX):
     """bf16 tensor [..., 128] -> (e4m3 codes uint8 [..., 128], fp32 descale [...]): per row
-    descale = amax / 448 (1 for a zero row), code = e4m3(x / descale)."""
+    descale = amax / 448 (1 for a zero row), rounded up to a power of two under
+    DESCALE_UE8M0; code = e4m3(x / descale)."""
     import torch
 
     if x.dtype != torch.bfloat16 or x.shape[-1] != 128 or not x.is_contiguous():
@@ -263,8 +272,8 @@ def quantize_rows(x, codes=None, descale=None, stream=None):
         codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
     if descale is None:
         descale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
-    st = lib().bsa_fp8_quantize_rows(_p(x), x.numel() // 128, _p(codes), _p(descale),
-                                     _stream_handle(stream))
+    fn = lib().bsa_fp8_quantize_rows_ue8m0 if rule == DESCALE_UE8M0 else lib().bsa_fp8_quantize_rows
+    st = fn(_p(x), x.numel() // 128, _p(codes), _p(descale), _stream_handle(stream))
     if st != 0:
         raise BsaError(st, "bsa_fp8_quantize_rows")
     return codes, descale
@@ -272,11 +281,12 @@ def quantize_rows(x, codes=None, descale=None, stream=None):
 
 def append_kv(k_new, v_new, cu_seqlens_new, cache_seqlens, block_table, k_pages, v_pages,
               k_descale=None, k_scale=None, v_scale=None, k_scale_kind=SCALE_PER_TOKEN_HEAD,
-              v_scale_kind=SCALE_PER_HEAD, dev_status=None, stream=None, kv_layout=KV_HND):
+              v_scale_kind=SCALE_PER_HEAD, dev_status=None, stream=None, kv_layout=KV_HND,
+              k_descale_rule: int = DESCALE_AMAX):
     """Writes bf16 K/V tokens [T_new, N2, 128] into the paged cache (k_pages / v_pages
     [P, N2, page_size, 128] (KV_HND) or [P, page_size, N2, 128] (KV_NHD) uint8 e4m3,
-    k_descale [P, N2, page_size] for per-token K) at positions cache_seqlens[b] + i through
-    block_table [B, L]; in place."""
+    k_descale [P, N2, page_size] for per-token K, computed under k_descale_rule) at positions
+    cache_seqlens[b] + i through block_table [B, L]; in place."""
     if kv_layout == KV_NHD:
         P, ps, N2, D = k_pages.shape
     else:
@@ -284,7 +294,7 @@ def append_kv(k_new, v_new, cu_seqlens_new, cache_seqlens, block_table, k_pages,
     dims = AppendDims(B=cu_seqlens_new.numel() - 1, N2=N2, D=D, page_size=ps, num_pages=P,
                       max_pages_per_seq=block_table.shape[1], total_new=k_new.shape[0],
                       k_scale_kind=k_scale_kind, v_scale_kind=v_scale_kind,
-                      kv_layout=int(kv_layout))
+                      kv_layout=int(kv_layout), k_descale_rule=int(k_descale_rule))
     st = lib().bsa_fp8_append_kv(ctypes.byref(dims), _p(k_new), _p(v_new), _p(cu_seqlens_new),
                                  _p(cache_seqlens), _p(block_table), _p(k_scale), _p(v_scale),
                                  _p(k_pages), _p(v_pages), _p(k_descale), _p(dev_status),

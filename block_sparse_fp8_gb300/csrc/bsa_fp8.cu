@@ -601,8 +601,8 @@ bsa_status_t quant_grid(Kernel kernel, long long rows, unsigned *grid) {
 
 }  // namespace
 
-extern "C" bsa_status_t bsa_fp8_quantize_rows(const void *x_bf16, long long rows,
-                                              void *codes_e4m3, float *descale, void *stream) {
+static bsa_status_t quantize_rows_impl(const void *x_bf16, long long rows, void *codes_e4m3,
+                                       float *descale, void *stream, bool ue8m0) {
   if (rows < 0) return BSA_ERR_INVALID_ARGUMENT;
   if (rows == 0) return BSA_OK;
   if (!x_bf16 || !codes_e4m3 || !descale || !aligned16(x_bf16) || !aligned16(codes_e4m3))
@@ -611,8 +611,20 @@ extern "C" bsa_status_t bsa_fp8_quantize_rows(const void *x_bf16, long long rows
   const bsa_status_t st = quant_grid(quant::quantize_rows_kernel, rows, &grid);
   if (st != BSA_OK) return st;
   quant::quantize_rows_kernel<<<grid, quant::THREADS, 0, (cudaStream_t)stream>>>(
-      static_cast<const uint4 *>(x_bf16), rows, static_cast<uint2 *>(codes_e4m3), descale);
+      static_cast<const uint4 *>(x_bf16), rows, static_cast<uint2 *>(codes_e4m3), descale,
+      ue8m0);
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+extern "C" bsa_status_t bsa_fp8_quantize_rows(const void *x_bf16, long long rows,
+                                              void *codes_e4m3, float *descale, void *stream) {
+  return quantize_rows_impl(x_bf16, rows, codes_e4m3, descale, stream, false);
+}
+
+extern "C" bsa_status_t bsa_fp8_quantize_rows_ue8m0(const void *x_bf16, long long rows,
+                                                    void *codes_e4m3, float *descale,
+                                                    void *stream) {
+  return quantize_rows_impl(x_bf16, rows, codes_e4m3, descale, stream, true);
 }
 
 extern "C" bsa_status_t bsa_fp8_append_kv(const bsa_fp8_append_dims_t *d, const void *k_new_bf16,
@@ -629,6 +641,8 @@ extern "C" bsa_status_t bsa_fp8_append_kv(const bsa_fp8_append_dims_t *d, const 
   if (d->v_scale_kind != BSA_SCALE_PER_HEAD && d->v_scale_kind != BSA_SCALE_PER_TENSOR)
     return BSA_ERR_INVALID_ARGUMENT;
   if (d->kv_layout != BSA_KV_HND && d->kv_layout != BSA_KV_NHD) return BSA_ERR_INVALID_ARGUMENT;
+  if (d->k_descale_rule != BSA_DESCALE_AMAX && d->k_descale_rule != BSA_DESCALE_UE8M0)
+    return BSA_ERR_INVALID_ARGUMENT;
   const long long rows = (long long)d->total_new * d->N2;
   if (rows == 0 || d->B == 0) return BSA_OK;
   const bool k_tok = d->k_scale_kind == BSA_SCALE_PER_TOKEN_HEAD;
@@ -662,6 +676,7 @@ extern "C" bsa_status_t bsa_fp8_append_kv(const bsa_fp8_append_dims_t *d, const 
   p.k_per_token = k_tok ? 1 : 0;
   p.v_per_head = d->v_scale_kind == BSA_SCALE_PER_HEAD ? 1 : 0;
   p.kv_nhd = d->kv_layout == BSA_KV_NHD ? 1 : 0;
+  p.k_ue8m0 = d->k_descale_rule == BSA_DESCALE_UE8M0 ? 1 : 0;
   quant::append_kv_kernel<<<grid, quant::THREADS, 0, (cudaStream_t)stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }

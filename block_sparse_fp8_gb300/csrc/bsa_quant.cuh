@@ -1,6 +1,7 @@
 // The quantise step before the attention call: bf16 rows of 128 values -> e4m3 codes and an
 // fp32 descale per row (FlashMLA page, section 量化 / 解量化的源码实现: scale = amax / 448,
-// stored value e4m3(x / scale)), and the K/V append into the paged cache.
+// stored value e4m3(x / scale); optionally the scale rounded up to a power of two, the same
+// section's cast to UE8M0), and the K/V append into the paged cache.
 //
 // HBM-bound.  A half-warp owns one 256-byte row: each lane loads 16 bytes (8 values), the row
 // maximum combines in four shuffles, and each lane stores its 8 codes (8 bytes), so a warp
@@ -78,14 +79,31 @@ __device__ __forceinline__ uint2 codes8(const float (&v)[8], float scale) {
   return make_uint2(e4m3x4(q[0], q[1], q[2], q[3]), e4m3x4(q[4], q[5], q[6], q[7]));
 }
 
-__device__ __forceinline__ float descale_of(float amax) {
-  return amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+// The smallest power of two not below x (x > 0, finite, below 2^127), from its bits: a
+// normal x with a zero fraction is one already, any other normal x goes to the next binade's
+// first value; a subnormal x is its fraction times 2^-149, so the power of two is the
+// fraction's, rounded up to the next power of two the same way.
+__device__ __forceinline__ float pow2_ceil(float x) {
+  const uint32_t b = __float_as_uint(x);
+  const uint32_t e = b & 0x7f800000u, m = b & 0x007fffffu;
+  if (m == 0u) return x;
+  if (e != 0u) return __uint_as_float(e + 0x00800000u);
+  return __uint_as_float((m & (m - 1u)) == 0u ? m : (1u << (32 - __clz(m))));
+}
+
+// descale of a row: amax / 448 (an fp32 quotient), or 1 for an all-zero row; with `ue8m0`
+// rounded up to a power of two (so that a code times its descale is exact).
+__device__ __forceinline__ float descale_of(float amax, bool ue8m0) {
+  if (!(amax > 0.f)) return 1.f;
+  const float d = __fdiv_rn(amax, 448.f);
+  return ue8m0 ? pow2_ceil(d) : d;
 }
 
 __global__ void __launch_bounds__(THREADS) quantize_rows_kernel(const uint4 *__restrict__ x,
                                                                 long long rows,
                                                                 uint2 *__restrict__ codes,
-                                                                float *__restrict__ descale) {
+                                                                float *__restrict__ descale,
+                                                                bool ue8m0) {
   const int lane = threadIdx.x & 15;
   const long long step = (long long)gridDim.x * (THREADS / 16);
   // every lane runs the same number of iterations (the shuffles need the whole warp); each
@@ -99,13 +117,13 @@ __global__ void __launch_bounds__(THREADS) quantize_rows_kernel(const uint4 *__r
     const uint4 w1 = live1 ? x[r1 * 16 + lane] : make_uint4(0, 0, 0, 0);
     float v[8];
     unpack8(w0, v);
-    const float d0 = descale_of(row_amax(v));
+    const float d0 = descale_of(row_amax(v), ue8m0);
     if (live0) {
       codes[r0 * 16 + lane] = codes8(v, d0);
       if (lane == 0) descale[r0] = d0;
     }
     unpack8(w1, v);
-    const float d1 = descale_of(row_amax(v));
+    const float d1 = descale_of(row_amax(v), ue8m0);
     if (live1) {
       codes[r1 * 16 + lane] = codes8(v, d1);
       if (lane == 0) descale[r1] = d1;
@@ -122,6 +140,7 @@ struct AppendParams {
   int *dev_status;
   int B, N2, ps, num_pages, L, total_new;
   int k_per_token, v_per_head, kv_nhd;
+  int k_ue8m0;  // per-token K descales rounded up to a power of two
 };
 
 // One warp per new token.  The token's first four heads of K and V are loaded before its
@@ -181,7 +200,7 @@ __global__ void __launch_bounds__(THREADS) append_kv_kernel(const AppendParams p
         // the shuffles of row_amax run on every lane, live or not
         const float amax = row_amax(v);
         if (live) {
-          const float d = p.k_per_token ? descale_of(amax) : p.k_scale[0];
+          const float d = p.k_per_token ? descale_of(amax, p.k_ue8m0) : p.k_scale[0];
           p.k_pages[row * 16 + hl] = codes8(v, d);
           if (p.k_per_token && hl == 0) p.k_descale[dst] = d;
           unpack8(wv[j], v);

@@ -57,7 +57,10 @@ typedef enum {
 /* Quantisation granularity of K and V (hpc-ops article, QuantType list):
  *   QPERTOKEN_PERHEAD_KPERTENSOR_VPERTENSOR      -> k: PER_TENSOR,     v: PER_TENSOR
  *   QPERTOKEN_PERHEAD_KPERTOKEN_PERHEAD_VPERHEAD -> k: PER_TOKEN_HEAD, v: PER_HEAD
- * Q is always per token per head. */
+ * The second type scales K per token group, head and dimension group.  The only dimension
+ * group the pages size is FlashMLA's 1 x 128 tile, which for a 128-wide head is the whole
+ * head; a token group's scale is given by repeating it over the group's tokens in the
+ * per-token array.  Q is always per token per head. */
 typedef enum {
   BSA_SCALE_PER_TENSOR = 0,     /* one fp32 scalar, k_descale[0] / v_descale[0] */
   BSA_SCALE_PER_TOKEN_HEAD = 1, /* K only: fp32 [num_pages, N2, page_size] */
@@ -260,7 +263,13 @@ bsa_status_t bsa_fp8_prefill_host(const bsa_fp8_dims_t *dims, const bsa_fp8_tens
  * at the granularities the attention pages give): descale = amax / 448 (largest finite
  * e4m3), computed in fp32, or 1 for an all-zero row; code = e4m3(x / descale) with an fp32
  * division, rounded to nearest even and saturated to +-448.  Inputs must be finite.
+ * With the UE8M0 rule (the same section's cast of the scale to UE8M0) the descale of a
+ * non-zero row is instead the smallest power of two not below amax / 448, so that code times
+ * descale is exact; the attention kernels take such descales like any other.
  * ------------------------------------------------------------------------------------------ */
+
+#define BSA_DESCALE_AMAX 0  /* descale = amax / 448 */
+#define BSA_DESCALE_UE8M0 1 /* descale = amax / 448 rounded up to a power of two */
 
 /* Quantises `rows` rows of 128 bf16 values (x_bf16 [rows, 128], e.g. Q [T, N1, 128] as
  * rows = T * N1) into codes_e4m3 [rows, 128] and one fp32 descale per row (descale [rows],
@@ -268,6 +277,10 @@ bsa_status_t bsa_fp8_prefill_host(const bsa_fp8_dims_t *dims, const bsa_fp8_tens
  * no-op.  Returns BSA_ERR_INVALID_ARGUMENT for null pointers, misalignment or rows < 0. */
 bsa_status_t bsa_fp8_quantize_rows(const void *x_bf16, long long rows, void *codes_e4m3,
                                    float *descale, void *stream);
+
+/* bsa_fp8_quantize_rows under the UE8M0 rule: same arguments, layouts and errors. */
+bsa_status_t bsa_fp8_quantize_rows_ue8m0(const void *x_bf16, long long rows, void *codes_e4m3,
+                                         float *descale, void *stream);
 
 typedef struct {
   int B;                 /* sequences */
@@ -281,13 +294,16 @@ typedef struct {
   bsa_scale_kind_t v_scale_kind; /* BSA_SCALE_PER_HEAD or BSA_SCALE_PER_TENSOR (given) */
   int kv_layout;         /* BSA_KV_HND (0): pages [P, N2, page_size, 128]; BSA_KV_NHD (1):
                             [P, page_size, N2, 128]; k_descale is [P, N2, page_size] in both */
+  int k_descale_rule;    /* BSA_DESCALE_AMAX (0) or BSA_DESCALE_UE8M0 (1): the computed
+                            per-token K descales (BSA_SCALE_PER_TOKEN_HEAD) */
 } bsa_fp8_append_dims_t;
 
 /* Appends new tokens to the paged K/V cache.  Token i of sequence b is row cu_seqlens_new[b]
  * + i of k_new_bf16 / v_new_bf16 [total_new, N2, 128] and lands at logical position
  * pos = cache_seqlens[b] + i: page block_table[b, pos / page_size], slot pos % page_size of
  * k_pages / v_pages (e4m3, HND or NHD pages as dims->kv_layout says).
- *   K, BSA_SCALE_PER_TOKEN_HEAD: each (token, head) row is quantised by the rule above and
+ *   K, BSA_SCALE_PER_TOKEN_HEAD: each (token, head) row is quantised by the rule above
+ *      (UE8M0 when dims->k_descale_rule says so) and
  *      its descale written to k_descale [P, N2, page_size] (k_scale unused, may be NULL).
  *   K, BSA_SCALE_PER_TENSOR: codes = e4m3(x / k_scale[0]) (k_descale unused, may be NULL).
  *   V: codes = e4m3(x / v_scale[head]) for BSA_SCALE_PER_HEAD (v_scale [N2]) or

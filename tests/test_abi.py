@@ -7,6 +7,8 @@ import os
 import re
 import shutil
 
+import numpy as np
+
 import pytest
 
 import block_sparse_fp8_gb300 as bsa
@@ -216,3 +218,37 @@ def test_host_call_empty_problem_is_a_no_op(L):
     nothing = {f"{s}.{n}": None for s in ("host", "dev") for n in bsa.TENSOR_NAMES}
     assert _host(L, _dims(B=0, total_q=0), **nothing) == 0
     assert _host(L, _dims(total_q=0), **nothing) == 0
+
+
+def test_append_descale_rule_checked(L):
+    fake = 0x10000
+    for rule, want in ((2, INVALID), (-1, INVALID)):
+        d = bsa.AppendDims(B=1, N2=2, D=128, page_size=64, num_pages=4, max_pages_per_seq=4,
+                           total_new=8, k_scale_kind=1, v_scale_kind=2, kv_layout=0,
+                           k_descale_rule=rule)
+        assert L.bsa_fp8_append_kv(ctypes.byref(d), *([fake] * 12)) == want
+
+
+def test_quantize_ue8m0_validation(L):
+    assert L.bsa_fp8_quantize_rows_ue8m0(None, 0, None, None, None) == 0
+    assert L.bsa_fp8_quantize_rows_ue8m0(None, -1, None, None, None) == INVALID
+    assert L.bsa_fp8_quantize_rows_ue8m0(0x10008, 4, 0x20000, 0x30000, None) == INVALID
+
+
+def test_generator_token_group_power_of_two_k_scales():
+    """The seeded generator's K scales per token group: one value per group of consecutive
+    tokens of a sequence and KV head, a power of two not below the group's amax / 448."""
+    import workloads as W
+
+    case = W.make_case("kg", 5, [300, 77], [300, 90], 4, 2, 32, W.SCALE_PER_TOKEN_HEAD,
+                       W.SCALE_PER_HEAD, "none", k_token_group=16, k_pow2=True,
+                       keep_logical=True)
+    kd = case.meta["k_descale_tok"]                           # [tokens, N2], token order
+    s0 = 0
+    for kv in (300, 90):
+        for g0 in range(0, kv, 16):
+            grp = kd[s0 + g0: s0 + min(kv, g0 + 16)]
+            assert np.all(grp == grp[0])
+        s0 += kv
+    lg = np.log2(kd.astype(np.float64))
+    assert np.all(lg == np.round(lg))

@@ -91,6 +91,28 @@ def test_attention_all_rows(name):
     assert not got.transpose(1, 0, 2)[empty].any()
 
 
+@pytest.mark.parametrize("ps,group", [(32, 16), (64, 64), (64, 128)])
+def test_k_scales_per_token_group_power_of_two(ps, group):
+    """The hpc-ops QuantType that scales K per token group, head and dimension group: one
+    power-of-two scale (FlashMLA's UE8M0 cast) per group of consecutive tokens and KV head,
+    the dimension group being the whole 128-wide head, given through the per-token K descale
+    array.  Strict exact band (0.5%) and the tight P-emulating band on every row."""
+    case = W.make_case(f"kgroup{group}_p{ps}", 112 + group, [700, 300], [700, 420], 8, 2, ps,
+                       W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD, "bernoulli", keep=0.5,
+                       k_token_group=group, k_pow2=True)
+    kd = case.k_descale[case.k_descale > 0].astype(np.float64)
+    assert np.all(np.log2(kd) == np.round(np.log2(kd)))
+    out, lse, st = run(case)
+    assert st == 0
+    orc = O.Oracle(case)
+    o_ex, l_ex, _ = orc.all_rows(O.EXACT)
+    o_pe, _, _ = orc.all_rows(O.PEMU)
+    got = out.float().cpu().numpy().astype(np.float64)
+    check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, "token-group K scales vs P-emulating")
+    check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, "token-group K scales vs exact")
+    check_lse(lse.cpu().numpy().astype(np.float64), l_ex, "token-group K scales lse")
+
+
 def test_heavy_outliers_follow_the_method():
     """5% of channels x8: e4m3 rounding of P alone (the P-emulating oracle) already puts
     ~0.8% of elements outside the exact band.  The kernel must sit in the tight band around

@@ -2,7 +2,8 @@
 
 bsa_fp8_quantize_rows (Q [T, N1, 128] bf16 -> e4m3 + q_descale) and bsa_fp8_append_kv (new
 K/V tokens into the paged cache) follow the FlashMLA page's quantisation rule (scale =
-amax / 448, stored value e4m3(x / scale)); codes are integers, so the bar is equality.
+amax / 448, stored value e4m3(x / scale)), and under the UE8M0 rule the same page's cast of
+the scale up to a power of two; codes are integers, so the bar is equality.
 """
 import numpy as np
 import pytest
@@ -31,35 +32,59 @@ def _rows(seed, n, scale=1.0):
     return f32_to_bf16_bits(x)
 
 
-def _gpu_quantize(xb):
+RULES = [O.DESCALE_AMAX, O.DESCALE_UE8M0]
+
+
+def _gpu_quantize(xb, rule=O.DESCALE_AMAX):
     import block_sparse_fp8_gb300 as bsa
 
     x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
-    codes, desc = bsa.quantize_rows(x)
+    codes, desc = bsa.quantize_rows(x, rule=rule)
     torch.cuda.synchronize()
     return codes.cpu().numpy(), desc.cpu().numpy()
 
 
-@pytest.mark.parametrize("n", [1, 15, 16, 17, 37, 1003])
-def test_quantize_rows_bit_exact(n):
-    _need_gpu()
-    xb = _rows(100 + n, n, scale=3.0)
-    codes, desc = _gpu_quantize(xb)
-    o_codes, o_desc = O.quantize_rows(xb)
-    assert np.array_equal(desc.view(np.uint32), o_desc.view(np.uint32))
+def _check_rows(xb, rule):
+    codes, desc = _gpu_quantize(xb, rule)
+    o_codes, o_desc = O.quantize_rows(xb, rule=rule)
+    assert np.array_equal(desc.view(np.uint32), o_desc.view(np.uint32)), \
+        f"{int((desc.view(np.uint32) != o_desc.view(np.uint32)).sum())} descales differ"
     assert np.array_equal(codes, o_codes), f"{int((codes != o_codes).sum())} codes differ"
 
 
-def test_quantize_rows_edge_values():
+@pytest.mark.parametrize("rule", RULES)
+@pytest.mark.parametrize("n", [1, 15, 16, 17, 37, 1003])
+def test_quantize_rows_bit_exact(n, rule):
     _need_gpu()
-    xb = _quant_rows_fixture()
-    codes, desc = _gpu_quantize(xb)
-    o_codes, o_desc = O.quantize_rows(xb)
-    assert np.array_equal(desc.view(np.uint32), o_desc.view(np.uint32))
-    assert np.array_equal(codes, o_codes)
+    _check_rows(_rows(100 + n, n, scale=3.0), rule)
 
 
-def test_quantize_rows_extreme_scales():
+@pytest.mark.parametrize("rule", RULES)
+def test_quantize_rows_edge_values(rule):
+    _need_gpu()
+    _check_rows(_quant_rows_fixture(), rule)
+
+
+def test_quantize_rows_ue8m0_subnormal_descales():
+    """Rows whose amax / 448 is an fp32 subnormal (amax down to the smallest bf16, 2^-133),
+    powers of two among them, and rows just above and at powers of two times 448."""
+    _need_gpu()
+    rows = []
+    for bits in (0x0001, 0x0002, 0x0003, 0x0005, 0x0010, 0x0011, 0x007F, 0x0080, 0x0081, 0x00FF,
+                 0x0100, 0x0123, 0x03FF, 0x0400, 0x0401):
+        r = np.zeros(128, dtype=np.uint16)
+        r[bits % 128] = bits
+        r[(bits + 5) % 128] = bits // 2 | 0x8000        # a smaller negative value
+        rows.append(r)
+    for e in (-20, -1, 0, 1, 7, 40):
+        for m in (448.0, 450.0, 446.0):
+            rows.append(f32_to_bf16_bits(np.full(128, m * 2.0 ** e, dtype=np.float32) *
+                                         np.linspace(-1, 1, 128, dtype=np.float32)))
+    _check_rows(np.stack(rows), O.DESCALE_UE8M0)
+
+
+@pytest.mark.parametrize("rule", RULES)
+def test_quantize_rows_extreme_scales(rule):
     """Rows whose descale lies outside and at the edges of the range where the kernel uses the
     corrected-reciprocal quotient (2^-90 .. 2^90) and so divides directly."""
     _need_gpu()
@@ -68,18 +93,10 @@ def test_quantize_rows_extreme_scales():
     base[:, 0] = 448.0                                     # amax 448 * 2^k -> descale 2^k
     exps = [-110, -91, -90, -89, 89, 90, 91, 110]
     x = np.stack([base[i] * np.float32(2.0 ** e) for i, e in enumerate(exps)])
-    xb = f32_to_bf16_bits(x)
-    codes, desc = _gpu_quantize(xb)
-    o_codes, o_desc = O.quantize_rows(xb)
-    assert np.array_equal(desc.view(np.uint32), o_desc.view(np.uint32))
-    assert np.array_equal(codes, o_codes)
+    _check_rows(f32_to_bf16_bits(x), rule)
     # non-power-of-two descales near both edges
     x2 = np.stack([base[i] * np.float32(1.37 * 2.0 ** e) for i, e in enumerate(exps)])
-    xb2 = f32_to_bf16_bits(x2)
-    codes, desc = _gpu_quantize(xb2)
-    o_codes, o_desc = O.quantize_rows(xb2)
-    assert np.array_equal(desc.view(np.uint32), o_desc.view(np.uint32))
-    assert np.array_equal(codes, o_codes)
+    _check_rows(f32_to_bf16_bits(x2), rule)
 
 
 def test_quantize_rows_full_q_of_the_bench_workload():
@@ -130,7 +147,7 @@ def _append_case(ps, k_kind, v_kind, seed=5):
                 k_scale=k_scale, v_scale=v_scale, k_kind=k_kind, v_kind=v_kind)
 
 
-def _run_append(c, nhd=False):
+def _run_append(c, nhd=False, rule=O.DESCALE_AMAX):
     """Runs the append; with nhd the cache is held as NHD pages and returned as HND."""
     import block_sparse_fp8_gb300 as bsa
 
@@ -144,7 +161,7 @@ def _run_append(c, nhd=False):
     bsa.append_kv(bf(c["kb"]), bf(c["vb"]), t(c["cu_new"]), t(c["cache_len"]), t(c["bt"]), kp, vp,
                   k_descale=kd, k_scale=t(c["k_scale"]), v_scale=t(c["v_scale"]),
                   k_scale_kind=c["k_kind"], v_scale_kind=c["v_kind"], dev_status=st,
-                  kv_layout=bsa.KV_NHD if nhd else bsa.KV_HND)
+                  kv_layout=bsa.KV_NHD if nhd else bsa.KV_HND, k_descale_rule=rule)
     torch.cuda.synchronize()
     kp, vp = kp.cpu().numpy(), vp.cpu().numpy()
     if nhd:
@@ -154,15 +171,16 @@ def _run_append(c, nhd=False):
 
 @pytest.mark.parametrize("nhd", [False, True])
 @pytest.mark.parametrize("ps", [32, 64])
-@pytest.mark.parametrize("kinds", [(W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD),
-                                   (W.SCALE_PER_TENSOR, W.SCALE_PER_TENSOR)])
+@pytest.mark.parametrize("kinds", [(W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD, O.DESCALE_AMAX),
+                                   (W.SCALE_PER_TOKEN_HEAD, W.SCALE_PER_HEAD, O.DESCALE_UE8M0),
+                                   (W.SCALE_PER_TENSOR, W.SCALE_PER_TENSOR, O.DESCALE_AMAX)])
 def test_append_kv_bit_exact(ps, kinds, nhd):
     _need_gpu()
-    c = _append_case(ps, *kinds)
-    kp, vp, kd, st = _run_append(c, nhd)
+    c = _append_case(ps, *kinds[:2])
+    kp, vp, kd, st = _run_append(c, nhd, rule=kinds[2])
     okp, ovp, okd, err = O.append_kv(c["kb"], c["vb"], c["cu_new"], c["cache_len"], c["bt"],
                                      c["kp"], c["vp"], c["kd"], c["k_kind"], c["v_kind"],
-                                     c["k_scale"], c["v_scale"])
+                                     c["k_scale"], c["v_scale"], k_descale_rule=kinds[2])
     assert st == 0 and err == 0
     assert np.array_equal(kp, okp), f"{int((kp != okp).sum())} K bytes differ"
     assert np.array_equal(vp, ovp), f"{int((vp != ovp).sum())} V bytes differ"
@@ -183,9 +201,11 @@ def test_append_kv_missing_page_reported_and_skipped():
     assert np.array_equal(kd.view(np.uint32), okd.view(np.uint32))
 
 
-def test_quantised_inputs_feed_the_prefill():
+@pytest.mark.parametrize("rule", RULES)
+def test_quantised_inputs_feed_the_prefill(rule):
     """bf16 Q/K/V -> quantise step on the GPU -> prefill; the result matches the oracle run on
-    the same quantised inputs (the formats of the two steps agree end to end)."""
+    the same quantised inputs (the formats of the two steps agree end to end), with the
+    descales of Q and K plain or rounded up to powers of two."""
     _need_gpu()
     import block_sparse_fp8_gb300 as bsa
     from gpu_helpers import EXACT_ATOL, EXACT_RTOL, MAX_OUTSIDE, band_fraction, to_device
@@ -206,9 +226,12 @@ def test_quantised_inputs_feed_the_prefill():
              kp=np.zeros((P, N2, ps, 128), np.uint8), vp=np.zeros((P, N2, ps, 128), np.uint8),
              kd=np.zeros((P, N2, ps), np.float32), k_scale=np.array([1.0], np.float32),
              v_scale=v_scale, k_kind=W.SCALE_PER_TOKEN_HEAD, v_kind=W.SCALE_PER_HEAD)
-    kp, vp, kd, st = _run_append(c)
-    q8, qd = _gpu_quantize(qb.reshape(-1, 128))
+    kp, vp, kd, st = _run_append(c, rule=rule)
+    q8, qd = _gpu_quantize(qb.reshape(-1, 128), rule)
     assert st == 0
+    if rule == O.DESCALE_UE8M0:
+        lg = np.log2(np.concatenate([qd.ravel(), kd[kd > 0]]).astype(np.float64))
+        assert np.all(lg == np.round(lg))
     base.q, base.q_descale = q8.reshape(q_len, N1, 128), qd.reshape(q_len, N1)
     base.k_pages, base.v_pages, base.k_descale, base.v_descale = kp, vp, kd, v_scale
     d = to_device(base)

@@ -257,8 +257,12 @@ def make_case(name: str, seed: int, q_lens, kv_lens, N1: int, N2: int, page_size
               sparse_frac: float = 0.25, n_empty: int = 0, n_local: int = 4,
               p_far: float = 0.05, softmax_scale: float | None = None,
               p_scale: float = 256.0, identity_pages: bool = False,
-              tail_fill: float | None = None, keep_logical: bool = False) -> Case:
-    """Builds a seeded case.  mask in {"bernoulli", "local_sink", "indices", "none", "ones"}."""
+              tail_fill: float | None = None, keep_logical: bool = False,
+              k_token_group: int = 1, k_pow2: bool = False) -> Case:
+    """Builds a seeded case.  mask in {"bernoulli", "local_sink", "indices", "none", "ones"}.
+    With a per-token K scale, k_token_group > 1 gives every group of that many consecutive
+    tokens of a sequence (per KV head) one scale, repeated over its tokens, and k_pow2 rounds
+    the scales up to powers of two."""
     B = len(q_lens)
     assert len(kv_lens) == B
     D = HEAD_DIM
@@ -322,7 +326,19 @@ def make_case(name: str, seed: int, q_lens, kv_lens, N1: int, N2: int, page_size
         k_desc = _amax_descale(np.array([np.abs(xk).max() if xk.size else 0.0]))
         k_codes = quantize_e4m3(xk, k_desc[0])
     elif k_scale_kind == SCALE_PER_TOKEN_HEAD:
-        kd_tok = _amax_descale(np.abs(xk).max(axis=2))          # [tot, N2]
+        amax = np.abs(xk).max(axis=2)                            # [tot, N2]
+        if k_token_group > 1:
+            s0 = 0
+            for kv in kv_lens:
+                for g0 in range(0, kv, k_token_group):
+                    grp = slice(s0 + g0, s0 + min(kv, g0 + k_token_group))
+                    amax[grp] = amax[grp].max(axis=0)
+                s0 += kv
+        kd_tok = _amax_descale(amax)
+        if k_pow2:
+            want = kd_tok.astype(np.float64)
+            p2 = np.exp2(np.ceil(np.log2(want)))
+            kd_tok = np.where(p2 < want, 2 * p2, p2).astype(np.float32)
         k_codes = quantize_e4m3(xk, kd_tok[:, :, None])
         k_desc = to_pages(kd_tok, fill=0)                        # [P, N2, ps]
     else:
