@@ -234,8 +234,9 @@ typedef struct {
  * each tensor `host` gives (the optional ones NULL in both, or given in both).  On `stream`
  * the call queues: one host-to-device copy per input tensor (host -> dev), the prefill on
  * the `dev` tensors exactly as bsa_fp8_prefill runs it, then the device-to-host copies of
- * O and, when given, the LSE (dev -> host).  It returns once they are queued; the host
- * outputs are valid after the stream has been synchronised.  Sizes come from `dims`:
+ * O and, when given, the LSE (dev -> host).  With page-locked host buffers it returns once
+ * they are queued; the host outputs are valid after the stream has been synchronised.  Sizes
+ * come from `dims`:
  *   q, out            T * N1 * 128 bytes (out: * 2, bf16)
  *   k_pages, v_pages  num_pages * N2 * page_size * 128 bytes
  *   q_descale         T * N1 floats;  lse  N1 * T floats
@@ -246,7 +247,9 @@ typedef struct {
  *   sparse_seq_len    B * N1 * Qb ints
  * Host buffers in page-locked memory (cudaHostAlloc / cudaHostRegister) make the copies
  * asynchronous, so that calls on two streams with separate `dev` sets and workspaces overlap
- * one call's copies with the other's prefill; pageable host memory gives the same results.
+ * one call's copies with the other's prefill.  Pageable host memory gives the same results,
+ * but the CUDA runtime may then hold the calling thread until a copy has completed (for the
+ * outputs, until the prefill has finished).
  * Every argument is checked, as bsa_fp8_prefill checks the `dev` set, before anything is
  * queued: BSA_ERR_INVALID_ARGUMENT for a NULL host pointer, a tensor given on one side only,
  * or what bsa_fp8_prefill rejects; BSA_ERR_CUDA if a copy cannot be queued.  `workspace` and
