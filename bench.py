@@ -761,11 +761,35 @@ def run_quantize(args, rank, world):
     ms = max_over_ranks([statistics.mean(per)], dev)[0]
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
+
+    # each kernel alone, timed the same way (after the timed region)
+    def alone(fn):
+        ts = []
+        for _ in range(max(5, min(args.steps, 20))):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    q_bytes = T * N1 * (256 + 128 + 4)
+    kv_bytes = nbytes - q_bytes
+    q_ms = alone(lambda: bsa.quantize_rows(q, q8, qd))
+    kv_ms = alone(lambda: bsa.append_kv(k, v, cu_new, cache_len, bt, k_pages, v_pages,
+                                        k_descale=k_desc, v_scale=v_scale, dev_status=status))
     if rank != 0:
         return None
     pk, src = peaks()
     hbm = pk.get("hbm_gbs", 6800.0)
     achieved = nbytes / (ms * 1e-3) / 1e9
+    per_kernel = {
+        name: {"ms_median": t, "bytes": b, "gbs": b / (t * 1e-3) / 1e9,
+               "frac": b / (t * 1e-3) / 1e9 / hbm}
+        for name, t, b in (("quantize_rows_kernel", q_ms, q_bytes),
+                           ("append_kv_kernel", kv_ms, kv_bytes))}
     return {
         "metric": "quantise step (bf16 Q rows -> e4m3 + descale, K/V append into pages) "
                   "HBM throughput",
@@ -782,6 +806,7 @@ def run_quantize(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": None,
                      "peak_source": f"{src}: copy bandwidth", "kernel": "quantize_rows + append_kv"},
+        "per_kernel": per_kernel,
         "gpu_launches": 2 * args.steps,
     }
 

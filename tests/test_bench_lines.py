@@ -65,3 +65,6 @@ def test_quantise_line():
     assert BASE_KEYS <= d.keys()
     assert d["value"] > 0 and d["roofline"]["bound"] == "hbm"
     assert d["config"]["op"] == "quantize" and d["gpu_launches"] == 6
+    pk = d["per_kernel"]
+    assert set(pk) == {"quantize_rows_kernel", "append_kv_kernel"}
+    assert sum(k["bytes"] for k in pk.values()) == d["config"]["bytes_per_step"]
