@@ -94,3 +94,28 @@ def test_host_call_macro_blocks_and_reused_buffers():
     assert st == 0
     assert torch.equal(h1, out1.cpu()) and torch.equal(l1, lse1.cpu())
     assert torch.equal(h2, out2.cpu()) and torch.equal(l2, lse2.cpu())
+
+
+def test_host_call_other_layouts():
+    """Q [N1, T, 128] with q_descale [N1, T] and NHD pages [P, page, N2, 128] from host
+    memory: the same copies (layout-independent sizes) and the TND / HND result bit for bit."""
+    import block_sparse_fp8_gb300 as bsa
+
+    case = W.make_case("bern_ragged", **SMALL["bern_ragged"])
+    ref_out, ref_lse, _ = run(case)
+    host = {n: torch.from_numpy(np.ascontiguousarray(getattr(case, n)))
+            for n in bsa.TENSOR_NAMES[:-2] if getattr(case, n) is not None}
+    host["q"] = host["q"].permute(1, 0, 2).contiguous()
+    host["q_descale"] = host["q_descale"].t().contiguous()
+    host["k_pages"] = host["k_pages"].permute(0, 2, 1, 3).contiguous()
+    host["v_pages"] = host["v_pages"].permute(0, 2, 1, 3).contiguous()
+    host["out"] = torch.zeros((case.T, case.N1, 128), dtype=torch.bfloat16)
+    host["lse"] = torch.zeros((case.N1, case.T))
+    host = {k: v.pin_memory() for k, v in host.items()}
+    dev = {k: torch.empty(v.shape, dtype=v.dtype, device="cuda") for k, v in host.items()}
+    bsa.prefill_host(host, dev, case.max_q_len, case.max_kv_len,
+                     softmax_scale=case.softmax_scale, p_scale=case.p_scale,
+                     causal=bool(case.causal), k_scale_kind=case.k_scale_kind,
+                     v_scale_kind=case.v_scale_kind, q_layout=bsa.Q_NTD, kv_layout=bsa.KV_NHD)
+    torch.cuda.synchronize()
+    assert torch.equal(host["out"], ref_out.cpu()) and torch.equal(host["lse"], ref_lse.cpu())
