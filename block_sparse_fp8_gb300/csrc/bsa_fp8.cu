@@ -372,7 +372,8 @@ bsa_status_t noalloc_scratch(void **addr) {
 
 // The prefill.  With `noalloc` it ignores workspace / workspace_bytes and uses the library's
 // own array instead (never split-KV); otherwise the caller's workspace must hold the split
-// plan's bytes.  With `check_only` it returns after every check, before anything is queued.
+// plan's bytes.  With `check_only` it returns after every check (the tensor maps' encoding
+// included), before anything is queued.
 static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, const void *k_pages,
                                  const void *v_pages, const float *q_descale,
                                  const float *k_descale, const float *v_descale,
@@ -422,7 +423,6 @@ static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, cons
   if (workspace_bytes < plan.bytes ||
       (plan.splits > 1 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
     return BSA_ERR_WORKSPACE;
-  if (check_only) return BSA_OK;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   p.splits = plan.splits;
   if (plan.splits > 1) {
@@ -477,6 +477,7 @@ static bsa_status_t prefill_impl(const bsa_fp8_dims_t *dims, const void *q, cons
     if (!encode_map(&tk, k_pages, 4, gd, gs, box)) return BSA_ERR_CUDA;
     if (!encode_map(&tv, v_pages, 4, gd, gs, box)) return BSA_ERR_CUDA;
   }
+  if (check_only) return BSA_OK;  // every check done, the tensor maps included
   // persistent grid: one CTA per SM (two pipelines each)
   const long long items = ntasks * plan.splits;
   const long long grid = std::min<long long>(items, (long long)per_sm * num_sms);
