@@ -42,13 +42,15 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("tiles_per_step", [1, 2])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_short_wait_limit_aborts_and_the_context_survives(name):
+def test_short_wait_limit_aborts_and_the_context_survives(name, tiles_per_step):
+    """Both kernels: one 128-token tile per online-softmax step, and 256-wide macro blocks."""
     import block_sparse_fp8_gb300 as bsa
 
     case = W.make_case(name, **CASES[name])
     d = to_device(case)
-    ref_out, ref_lse, st = run(case, d)
+    ref_out, ref_lse, st = run(case, d, tiles_per_step=tiles_per_step)
     assert st == 0
     rows = sample_rows(case, 2048, seed=9)
     o_ex, l_ex, err = O.Oracle(case).rows(rows, O.EXACT)
@@ -58,12 +60,12 @@ def test_short_wait_limit_aborts_and_the_context_survives(name):
     bsa.set_wait_limit_ns(1000)
     try:
         for i in range(3):
-            _, _, st = run(case, d)
+            _, _, st = run(case, d, tiles_per_step=tiles_per_step)
             assert st & bsa.DEV_TIMEOUT, f"launch {i}: no wait ran out (status {st})"
             assert st & ~bsa.DEV_TIMEOUT == 0, f"launch {i}: status {st}"
     finally:
         bsa.set_wait_limit_ns(0)
-    out, lse, st = run(case, d)
+    out, lse, st = run(case, d, tiles_per_step=tiles_per_step)
     assert st == 0
     assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
     check_lse(lse[rows[:, 1], rows[:, 0]].cpu().numpy(), l_ex, f"{name} after")
