@@ -113,3 +113,26 @@ def test_grouping_is_the_one_asked_for(tiles_per_step):
     got = out.float().cpu().numpy()[255, 0]
     assert np.all(np.abs(got - mine[255, 0]) <= 0.004 * np.abs(mine[255, 0]))
     assert np.all(np.abs(got - other[255, 0]) > 0.006 * np.abs(other[255, 0]))
+
+
+def test_macro_block_longest_supported_kv():
+    """Kb = 4096 KV tiles with two list tiles per step: the longest list the one-pipeline kernel
+    holds in shared memory (it never splits), sampled rows against the exact formula and the
+    pair-P-emulating mode."""
+    from gpu_helpers import sample_rows
+
+    case = W.make_case("max_kb", 301, [256], [4096 * 128], 2, 1, 64, W.SCALE_PER_TOKEN_HEAD,
+                       W.SCALE_PER_HEAD, "local_sink", n_local=2, p_far=0.01)
+    assert case.Kb == 4096
+    d = to_device(case)
+    out, lse, st = run(case, d, tiles_per_step=2)
+    assert st == 0
+    rows = sample_rows(case, 96, seed=3)
+    orc = O.Oracle(case)
+    o_ex, l_ex, err = orc.rows(rows, O.EXACT)
+    o_pe, _, _ = orc.rows(rows, O.PEMU, group=2)
+    assert err == 0
+    got = out.float()[rows[:, 0], rows[:, 1]].cpu().numpy()
+    check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, "max Kb, two tiles per step, vs exact")
+    check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, "max Kb vs P-emulating, two tiles per step")
+    check_lse(lse[rows[:, 1], rows[:, 0]].cpu().numpy(), l_ex, "max Kb lse, two tiles per step")
