@@ -185,6 +185,9 @@ def _small_cases():
         W.make_case("qlong", 15, [300], [170], 2, 1, 64, mask="ones", keep_logical=True),
         W.make_case("noncausal", 16, [200, 140], [330, 140], 4, 2, 32, W.SCALE_PER_TOKEN_HEAD,
                     W.SCALE_PER_HEAD, "ones", causal=0, keep_logical=True),
+        # a sequence with no KV tokens at all: every row of it sees no key
+        W.make_case("kv0", 17, [200, 130], [0, 300], 4, 2, 64, W.SCALE_PER_TOKEN_HEAD,
+                    W.SCALE_PER_HEAD, "bernoulli", keep=0.6, keep_logical=True),
     ]
 
 

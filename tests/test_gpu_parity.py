@@ -113,6 +113,29 @@ def test_k_scales_per_token_group_power_of_two(ps, group):
     check_lse(lse.cpu().numpy().astype(np.float64), l_ex, "token-group K scales lse")
 
 
+@pytest.mark.parametrize("causal", [1, 0])
+def test_sequence_without_kv(causal):
+    """A sequence with kv_len = 0 beside a normal one: its tasks have no tile, every row of it
+    gives O = 0 exactly and LSE = -FLT_MAX; the other sequence is unaffected."""
+    case = W.make_case("kv0", 17, [200, 130], [0, 300], 4, 2, 64, W.SCALE_PER_TOKEN_HEAD,
+                       W.SCALE_PER_HEAD, "bernoulli", keep=0.6, causal=causal)
+    ref_l, ref_c, _ = O.Oracle(case).lists()
+    lists, counts, st = run_lists(case)
+    assert st == 0 and np.array_equal(counts, ref_c) and np.array_equal(lists, ref_l)
+    out, lse, st = run(case)
+    assert st == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    gl = lse.cpu().numpy().astype(np.float64)
+    assert not got[:200].any()
+    assert np.all(gl[:, :200] == np.float32(NEG_FLT_MAX))
+    orc = O.Oracle(case)
+    o_ex, l_ex, _ = orc.all_rows(O.EXACT)
+    o_pe, _, _ = orc.all_rows(O.PEMU)
+    check_o(got, o_pe, PEMU_ATOL, PEMU_RTOL, "kv0 vs P-emulating")
+    check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, "kv0 vs exact")
+    check_lse(gl, l_ex, "kv0 lse")
+
+
 def test_heavy_outliers_follow_the_method():
     """5% of channels x8: e4m3 rounding of P alone (the P-emulating oracle) already puts
     ~0.8% of elements outside the exact band.  The kernel must sit in the tight band around
