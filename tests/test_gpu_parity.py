@@ -136,6 +136,24 @@ def test_sequence_without_kv(causal):
     check_lse(gl, l_ex, "kv0 lse")
 
 
+def test_sequence_without_queries():
+    """A sequence with q_len = 0 first (its KV pages exist but no task reads them), one with
+    kv_len = 0 and a normal one; index lists, page 32.  Lists bit-exact, every row against the
+    oracle."""
+    case = W.make_case("q0", 18, [0, 200, 130], [90, 0, 300], 4, 2, 32, W.SCALE_PER_TOKEN_HEAD,
+                       W.SCALE_PER_HEAD, "indices", sparse_frac=0.5)
+    ref_l, ref_c, _ = O.Oracle(case).lists()
+    lists, counts, st = run_lists(case)
+    assert st == 0 and np.array_equal(counts, ref_c) and np.array_equal(lists, ref_l)
+    out, lse, st = run(case)
+    assert st == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    o_ex, l_ex, _ = O.Oracle(case).all_rows(O.EXACT)
+    check_o(got, o_ex, EXACT_ATOL, EXACT_RTOL, "q0 vs exact")
+    check_lse(lse.cpu().numpy().astype(np.float64), l_ex, "q0 lse")
+    assert not got[:200].any()
+
+
 def test_heavy_outliers_follow_the_method():
     """5% of channels x8: e4m3 rounding of P alone (the P-emulating oracle) already puts
     ~0.8% of elements outside the exact band.  The kernel must sit in the tight band around
