@@ -622,9 +622,11 @@ def run_ours(args, rank, world):
         line["roofline"]["kernel"] = "bsa_attention_wide_kernel"
     if macro is not None:
         line["macro_block_256"] = macro_line(macro, flops, fp8_peak)
-    if not args.no_cpu_baseline and world >= 1:
+    # the CPU baseline and the other workloads belong to the one-GPU line: under torchrun the
+    # other ranks have finished and would wait on rank 0 for them
+    if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(case, lists, counts, args.cpu_seconds)
-    if not args.no_others and args.batch == 0:
+    if not args.no_others and args.batch == 0 and world == 1:
         # the other full-size workloads, one after the other on this GPU (not part of the
         # timed region above)
         del d, out, lse
